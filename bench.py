@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MLA decode hot path on GB300.
+
+One step = one whole decode call (split kernel + combine kernel) for the
+batch-32 / 64-head / top-2048 workload (65536 cached rows per sequence, half the
+picks from the last 4096 positions), inputs resident in HBM.  Between steps the
+L2 is flushed (a 256 MiB write) and the index set rotates over 8 independent draws,
+so every step reads its rows from HBM.  Each step is timed with CUDA events on the
+launching stream; the split kernel is also timed on its own (events around it) for
+the roofline line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  With N > 1 (torchrun) every rank runs an independent replica
+of the workload on its own GPU (no data exchange); `value` is the total over ranks.
+`--impl reference` times the CPU float64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mla_decode_03_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode queries/s and gathered-KV GB/s (% of HBM and tensor-pipe roofline)"
+UNIT = "queries/s"
+WORKLOAD = "c3"
+N_INDEX_SETS = 8
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_inputs(w, device):
+    """Host copies of q bits and of the rows the queries reference (compact)."""
+    L = W.seq_lengths(w)
+    kv = W.make_cache(w, L, device=device)
+    q = W.make_q(w, device=device)
+    idx = W.make_indices(w, L)
+    rows, remap = W.compact_rows(kv, idx)
+    qbits = W.bf16_bits(q)
+    del kv
+    return qbits, rows, remap
+
+
+def time_oracle(qbits, rows, remap, scale, budget_s: float, max_queries: int = 1 << 30):
+    """Runs the oracle query by query (cycling over the batch) for about budget_s."""
+    import oracle.mla_oracle as O
+    B = qbits.shape[0]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b = done % B
+        O.sparse_mla_decode(qbits[b:b + 1], rows, remap[b:b + 1], scale)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= max_queries:
+            return done, el
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    w = W.WORKLOADS[WORKLOAD]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    qbits, rows, remap = oracle_inputs(w, dev)
+    per_step_s = 2.0
+    time_oracle(qbits, rows, remap, w.softmax_scale, 0.0, max_queries=max(1, args.warmup))
+    total_q, total_t, step_ms = 0, 0.0, []
+    for _ in range(args.steps):
+        n, el = time_oracle(qbits, rows, remap, w.softmax_scale, per_step_s)
+        total_q += n
+        total_t += el
+        step_ms.append(1e3 * el / n * w.batch)
+    value = total_q / total_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{total_q} queries of the workload, about {per_step_s:.0f} s "
+                                   f"of oracle work per step, one query per call"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def config_dict(w, S):
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "topk": w.topk,
+            "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
+            "row_bytes": W.ROW_BYTES, "num_splits": S,
+            "index_sets": N_INDEX_SETS,
+            "l2": "flushed between steps (256 MiB write) + 8 rotating index sets"}
+
+
+def run_gpu(args):
+    import sparse_mla_decode_03_gb300 as smla
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = W.WORKLOADS[WORKLOAD]
+    L = W.seq_lengths(w)
+    seed = w.seed + 7919 * rank
+    kv = W.make_cache(w, L, device=dev, gen_seed=seed)
+    q = W.make_q(w, device=dev, gen_seed=seed)
+    idx_np = [W.make_indices(w, L, variant=v + 100 * rank) for v in range(N_INDEX_SETS)]
+    idx_sets = [torch.as_tensor(i, device=dev) for i in idx_np]
+    B, H = w.batch, w.heads
+    params = smla.make_params(B, H, w.topk, kv.shape[0], kv.stride(0), w.softmax_scale)
+    S = smla.smla_default_num_splits(params)
+    o_part = torch.empty((B, H, S, 448), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    out = torch.empty((B, H, 448), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
+                                     o_part=o_part, lse_part=lse_part, stream=stream)
+        smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse, stream=stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize(dev)
+    if smla.smla_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
+                                     o_part=o_part, lse_part=lse_part, stream=stream)
+        e1.record(stream)
+        smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse, stream=stream)
+        e2.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    split_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    ms = statistics.mean(step_ms)
+    split_mean = statistics.mean(split_ms)
+
+    # ---- end to end through the C ABI, host buffers, copies inside the timed region ----
+    q_h = q.cpu().pin_memory()
+    idx_h = [i.cpu().pin_memory() for i in idx_sets]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(q)
+    idx_d = torch.empty_like(idx_sets[0])
+    ws_bytes = smla.smla_workspace_size(params, S)
+    wspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    Ke = max(10, K // 4)
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+    for i in range(3 + Ke):
+        flush.zero_()
+        if i >= 3:
+            ee[i - 3][0].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h[i % N_INDEX_SETS], non_blocking=True)
+        smla.sparse_mla_decode(q_d, kv, idx_d, w.softmax_scale, out=out, lse=lse, num_splits=S,
+                               workspace=wspace, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        if i >= 3:
+            ee[i - 3][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ee)
+    h2d = q.numel() * q.element_size() + idx_sets[0].numel() * 4
+    d2h = out.numel() * out.element_size() + lse.numel() * 4
+
+    # ---- aggregate over ranks ----
+    if ws > 1:
+        t = torch.tensor([ms, split_mean, e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, split_mean, e2e_ms = t.tolist()
+    value = ws * B / (ms * 1e-3)
+    e2e_value = ws * B / (e2e_ms * 1e-3)
+
+    hbm_peak, tc_peak, peak_kind = read_peaks()
+    mean_valid_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
+    split_bytes = mean_valid_bytes + q.numel() * 2 + B * w.topk * 4
+    achieved = split_bytes / (split_mean * 1e-3) / 1e9
+    flops = statistics.mean(W.algorithmic_flops(w, i) for i in idx_np)
+    tc_achieved = flops / (split_mean * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, S),
+        "gathered_kv_gbs": ws * mean_valid_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_source": f"hbm_gbs ({peak_kind})", "traffic": None,
+                     "algorithmic_bytes_per_launch": split_bytes,
+                     "launch_ms": split_mean,
+                     "tensor_frac": tc_achieved / tc_peak,
+                     "tensor_tflops": tc_achieved},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        qb = W.bf16_bits(q)
+        rows, remap = W.compact_rows(kv, idx_np[0])
+        del kv
+        n, el = time_oracle(qb, rows, remap, w.softmax_scale, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": f"{n} queries of the same workload (cycling over the "
+                                          f"batch of {B}), {el:.1f} s, numpy float64"}
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

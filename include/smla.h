@@ -1,0 +1,135 @@
+/*
+ * smla.h -- C ABI of the GB300 (sm_103a) sparse MLA decode library (libsmla.so).
+ *
+ * The operation.  Sparse Multi-head Latent Attention decode: for every decode
+ * query b and head h, softmax attention over the top-k KV-cache rows selected for
+ * that query, all heads sharing one gathered read of the rows ("The Moment of
+ * Compilation: When a Triton Kernel Meets Its Constraints", section "The Context:
+ * A Kernel Optimization Campaign": one KV read shared by all heads, scores for all
+ * heads in one batched matrix product).  Row format ("The Power-of-Two Trap:
+ * Debugging a Triton MMA Kernel on Blackwell GPUs", sections "3. The Scale
+ * Indexing Complication" and "Input Knowledge Required"), 584 bytes per row:
+ *
+ *     [0,448)   FP8 e4m3 nope values        k_nope[c] = e4m3(byte c) * 2^(s[c/64]-127)
+ *     [448,455) UE8M0 scale of each 64-column group s[0..6]
+ *     455       padding byte (never used)
+ *     [456,584) 64 bf16 rope values (little endian)
+ *
+ * With q = bf16 [512] = q_nope[448] | q_rope[64] and scale = softmax_scale:
+ *     score[t] = scale * (q_nope . k_nope[t] + q_rope . k_rope[t])
+ *     lse      = ln sum_t exp(score[t])
+ *     out      = sum_t exp(score[t] - lse) * k_nope[t]          (448 wide)
+ * over the valid (>= 0) indices of the query; no valid index gives out = 0 and
+ * lse = -inf.  The split-K form ("The 80KB Mystery: Resolving Contradictory
+ * Evidence in Triton Kernel Optimization", section "The Context: Optimizing
+ * Attention on Blackwell": the top-k is partitioned across CTAs, nsplit) computes
+ * the same quantities per split of the index list, and the combine merges them:
+ *     lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * out_s.
+ *
+ * Conventions common to every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library keeps
+ *     no pointer after a call returns and allocates no device or host memory.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  They do not
+ *     synchronise the host and allocate nothing, so they may be captured in a CUDA
+ *     graph once the device has been initialised by one eager call.
+ *   - Layouts are dense, row-major, with the shapes given.  bf16 means IEEE
+ *     bfloat16 bit patterns (uint16).
+ *   - Return value: SMLA_OK (0) or a negative smla_status.  Argument errors are
+ *     detected on the host before any launch; nothing is launched then.
+ *   - Index values >= num_rows violate the contract.  The kernels never read such a
+ *     row: they treat it as masked and record SMLA_ERR_INDEX_RANGE in the device
+ *     status word (see smla_device_status).
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* smla_stream_t; /* == cudaStream_t */
+
+enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = -1,        /* null pointer, bad alignment, bad size          */
+  SMLA_ERR_UNSUPPORTED_SHAPE = -2,  /* num_heads not in {16, 32, 64, 128}, ...        */
+  SMLA_ERR_WORKSPACE_TOO_SMALL = -3,
+  SMLA_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
+  SMLA_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed           */
+  SMLA_ERR_TIMEOUT = -6,            /* device status: a bounded wait in a kernel ran out */
+  SMLA_ERR_INDEX_RANGE = -7,        /* device status: an index >= num_rows was skipped */
+};
+
+/* Problem description shared by the entry points. */
+typedef struct smla_params {
+  int32_t batch;          /* B: decode queries (one token each), >= 1                  */
+  int32_t num_heads;      /* H: query heads, one of 16, 32, 64, 128                    */
+  int32_t topk;           /* k: index slots per query, 1 .. 65536                      */
+  int32_t reserved;       /* must be 0                                                 */
+  int64_t num_rows;       /* rows in kv_cache, >= 1                                    */
+  int64_t kv_row_stride;  /* bytes between consecutive rows, >= 584, multiple of 8      */
+  float softmax_scale;    /* multiplies q.k (e.g. 1/sqrt(512)), finite and > 0          */
+} smla_params;
+
+/* Number of splits the library would use for `p` on the current device (its plan:
+ * enough CTAs to fill the device's SMs, splits aligned to 16 index slots).  */
+int smla_default_num_splits(const smla_params* p, int32_t* num_splits);
+
+/* Workspace bytes sparse_mla_decode needs with `num_splits` splits (0 = the default
+ * plan).  The workspace holds the split partials: fp32 o_part [B, H, S, 448] and
+ * fp32 lse_part [B, H, S], each 256-byte aligned. */
+int smla_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes);
+
+/*
+ * One whole decode step: split kernel + combine kernel.
+ *   q          bf16  [B, H, 512]  (448 nope | 64 rope), 16-byte aligned
+ *   kv_cache   uint8 [num_rows, kv_row_stride], 16-byte aligned, rows as above
+ *   indices    int32 [B, topk]    row ids; < 0 = masked slot (shared by all heads)
+ *   out        bf16  [B, H, 448]  16-byte aligned
+ *   lse        fp32  [B, H]       natural-log LSE of the scaled scores (-inf if empty)
+ *   workspace  device scratch of >= smla_workspace_size(p, num_splits) bytes,
+ *              256-byte aligned; its contents on entry do not matter
+ *   num_splits 0 = default plan, else 1 .. min(256, ceil(topk / 16))
+ */
+int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indices,
+                      void* out, float* lse, const smla_params* p, int32_t num_splits,
+                      void* workspace, size_t workspace_bytes, smla_stream_t stream);
+
+/*
+ * Split kernel alone.  Split s covers index positions [16*g0, min(16*g1, topk)) with
+ * G = ceil(topk/16), g0 = s*G/S, g1 = (s+1)*G/S (integer division); a split may be
+ * empty.  Writes, per split, the normalised partial attention and its LSE:
+ *   o_part   fp32 [B, H, S, 448]   (0 where the split has no valid index)
+ *   lse_part fp32 [B, H, S]        (-inf where the split has no valid index)
+ * num_splits: 1 .. min(256, ceil(topk / 16)).
+ */
+int sparse_mla_decode_split(const void* q, const void* kv_cache, const int32_t* indices,
+                            const smla_params* p, int32_t num_splits, float* o_part,
+                            float* lse_part, smla_stream_t stream);
+
+/*
+ * Combine kernel alone: merges S split partials per (b, h) with log-sum-exp weights.
+ *   o_part fp32 [B, H, S, 448], lse_part fp32 [B, H, S]  (as written by the split call)
+ *   out bf16 [B, H, 448] (16-byte aligned), lse fp32 [B, H]
+ * Splits with lse_part = -inf carry no weight; all -inf gives out = 0, lse = -inf.
+ * 1 <= S <= 1024.
+ */
+int sparse_mla_combine(const float* o_part, const float* lse_part, int32_t batch,
+                       int32_t num_heads, int32_t num_splits, void* out, float* lse,
+                       smla_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* smla_status_string(int status);
+
+/* Reads the current device's status word, which kernels set (first error wins) when
+ * a bounded wait runs out (SMLA_ERR_TIMEOUT) or an index is out of range
+ * (SMLA_ERR_INDEX_RANGE).  Synchronises the device.  clear != 0 resets it to 0. */
+int smla_device_status(int32_t* status, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMLA_H_ */

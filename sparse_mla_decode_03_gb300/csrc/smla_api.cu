@@ -1,0 +1,225 @@
+// C ABI of libsmla.so: argument validation, split planning and kernel launches.
+// Declarations and their documentation are in include/smla.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/smla.h"
+#include "smla_internal.h"
+
+namespace {
+
+using smla::kMaxCombineSplits;
+using smla::kMaxSplits;
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};  // 0 = not queried yet, -1 = unsupported device
+
+// SM count of the current device, or an error status if it is not sm_103.
+int current_device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SMLA_ERR_UNSUPPORTED_DEVICE;
+  if (g_sm_count[dev] == 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    g_sm_count[dev] = (major == 10 && minor == 3) ? n : -1;
+  }
+  if (g_sm_count[dev] < 0) return SMLA_ERR_UNSUPPORTED_DEVICE;
+  *sms = g_sm_count[dev];
+  return SMLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_params(const smla_params* p) {
+  if (p == nullptr) return SMLA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->topk < 1 || p->topk > 65536 || p->num_rows < 1 || p->reserved != 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (p->kv_row_stride < smla::kRowBytes || (p->kv_row_stride % 8) != 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.f)) return SMLA_ERR_INVALID_ARG;
+  if (p->num_heads != 16 && p->num_heads != 32 && p->num_heads != 64 && p->num_heads != 128)
+    return SMLA_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(p->batch) * p->num_heads > (int64_t(1) << 30))
+    return SMLA_ERR_UNSUPPORTED_SHAPE;
+  return SMLA_OK;
+}
+
+int max_splits(const smla_params* p) {
+  const int granules = (p->topk + 15) / 16;
+  return granules < kMaxSplits ? granules : kMaxSplits;
+}
+
+// Plan: 1 CTA per SM is resident (the kernel uses ~210 KB of shared memory), so
+// choose S to minimise (waves of CTAs) x (128-token tiles per CTA + a fixed
+// per-CTA overhead of about a third of a tile), preferring fewer splits on ties.
+int plan_splits(const smla_params* p, int sms) {
+  const int groups = p->num_heads > 64 ? p->num_heads / 64 : 1;
+  const int64_t ctas_per_split = static_cast<int64_t>(p->batch) * groups;
+  const int smax = max_splits(p);
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= smax; ++s) {
+    const int granules = (p->topk + 15) / 16;
+    const int gmax = (granules + s - 1) / s;              // granules of the largest split
+    const int tiles = (gmax * 16 + 127) / 128;
+    const int64_t waves = (ctas_per_split * s + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (tiles + 0.35);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+void workspace_layout(const smla_params* p, int S, size_t* o_bytes, size_t* total) {
+  const size_t bhs = static_cast<size_t>(p->batch) * p->num_heads * S;
+  *o_bytes = round256(bhs * smla::kNope * sizeof(float));
+  *total = *o_bytes + round256(bhs * sizeof(float));
+}
+
+int resolve_splits(const smla_params* p, int32_t requested, int* S) {
+  if (requested < 0) return SMLA_ERR_INVALID_ARG;
+  if (requested == 0) {
+    int sms = 0;
+    const int st = current_device_sms(&sms);
+    if (st != SMLA_OK) return st;
+    *S = plan_splits(p, sms);
+    return SMLA_OK;
+  }
+  if (requested > max_splits(p)) return SMLA_ERR_INVALID_ARG;
+  *S = requested;
+  return SMLA_OK;
+}
+
+int check_tensors(const void* q, const void* kv, const int32_t* idx) {
+  if (q == nullptr || kv == nullptr || idx == nullptr) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(idx, 4)) return SMLA_ERR_INVALID_ARG;
+  return SMLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int smla_default_num_splits(const smla_params* p, int32_t* num_splits) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  if (num_splits == nullptr) return SMLA_ERR_INVALID_ARG;
+  int S = 0;
+  st = resolve_splits(p, 0, &S);
+  if (st != SMLA_OK) return st;
+  *num_splits = S;
+  return SMLA_OK;
+}
+
+int smla_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  if (bytes == nullptr) return SMLA_ERR_INVALID_ARG;
+  int S = 0;
+  st = resolve_splits(p, num_splits, &S);
+  if (st != SMLA_OK) return st;
+  size_t o_bytes = 0, total = 0;
+  workspace_layout(p, S, &o_bytes, &total);
+  *bytes = total;
+  return SMLA_OK;
+}
+
+int sparse_mla_decode_split(const void* q, const void* kv_cache, const int32_t* indices,
+                            const smla_params* p, int32_t num_splits, float* o_part,
+                            float* lse_part, smla_stream_t stream) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  st = check_tensors(q, kv_cache, indices);
+  if (st != SMLA_OK) return st;
+  if (o_part == nullptr || lse_part == nullptr || !aligned(o_part, 16) || !aligned(lse_part, 4))
+    return SMLA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > max_splits(p)) return SMLA_ERR_INVALID_ARG;
+  int sms = 0;
+  st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  const cudaError_t e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
+                                           p->num_heads, p->topk, num_splits, p->num_rows,
+                                           p->kv_row_stride, p->softmax_scale,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+int sparse_mla_combine(const float* o_part, const float* lse_part, int32_t batch,
+                       int32_t num_heads, int32_t num_splits, void* out, float* lse,
+                       smla_stream_t stream) {
+  if (o_part == nullptr || lse_part == nullptr || out == nullptr || lse == nullptr)
+    return SMLA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 8) || !aligned(lse_part, 4) || !aligned(out, 16) || !aligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  if (batch < 1 || num_heads < 1 || num_splits < 1 || num_splits > kMaxCombineSplits)
+    return SMLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * num_heads > (int64_t(1) << 30))
+    return SMLA_ERR_UNSUPPORTED_SHAPE;
+  int sms = 0;
+  const int st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  const cudaError_t e = smla::launch_combine(o_part, lse_part, batch, num_heads, num_splits, out,
+                                             lse, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indices, void* out,
+                      float* lse, const smla_params* p, int32_t num_splits, void* workspace,
+                      size_t workspace_bytes, smla_stream_t stream) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  st = check_tensors(q, kv_cache, indices);
+  if (st != SMLA_OK) return st;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  int S = 0;
+  st = resolve_splits(p, num_splits, &S);
+  if (st != SMLA_OK) return st;
+  size_t o_bytes = 0, total = 0;
+  workspace_layout(p, S, &o_bytes, &total);
+  if (workspace == nullptr || !aligned(workspace, 256)) return SMLA_ERR_INVALID_ARG;
+  if (workspace_bytes < total) return SMLA_ERR_WORKSPACE_TOO_SMALL;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
+                                     p->num_heads, p->topk, S, p->num_rows, p->kv_row_stride,
+                                     p->softmax_scale, s);
+  if (e != cudaSuccess) return SMLA_ERR_CUDA;
+  e = smla::launch_combine(o_part, lse_part, p->batch, p->num_heads, S, out, lse, s);
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+const char* smla_status_string(int status) {
+  switch (status) {
+    case SMLA_OK: return "SMLA_OK";
+    case SMLA_ERR_INVALID_ARG: return "SMLA_ERR_INVALID_ARG: invalid argument";
+    case SMLA_ERR_UNSUPPORTED_SHAPE: return "SMLA_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+    case SMLA_ERR_WORKSPACE_TOO_SMALL: return "SMLA_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case SMLA_ERR_UNSUPPORTED_DEVICE:
+      return "SMLA_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+    case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA: CUDA runtime error";
+    case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+    case SMLA_ERR_INDEX_RANGE: return "SMLA_ERR_INDEX_RANGE: an index >= num_rows was skipped";
+    default: return "SMLA: unknown status";
+  }
+}
+
+int smla_device_status(int32_t* status, int32_t clear) {
+  if (status == nullptr) return SMLA_ERR_INVALID_ARG;
+  int sms = 0;
+  const int st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  return smla::read_device_status(status, clear != 0) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,27 @@
+// Host-side interface between the C ABI layer (smla_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace smla {
+
+constexpr int kQkDim = 512;     // q / k width: 448 nope + 64 rope
+constexpr int kNope = 448;      // value / output width
+constexpr int kRowBytes = 584;  // packed KV row
+constexpr int kMaxSplits = 256;
+constexpr int kMaxCombineSplits = 1024;
+
+// Launches the split kernel: grid (S, H / heads_per_cta, B), 128 threads.
+cudaError_t launch_split(const void* q, const void* kv, const int32_t* indices, float* o_part,
+                         float* lse_part, int B, int H, int topk, int S, int64_t num_rows,
+                         int64_t stride, float softmax_scale, cudaStream_t stream);
+
+// Launches the combine kernel over B * H (batch, head) pairs.
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int H, int S,
+                           void* out, float* lse, cudaStream_t stream);
+
+// Device status word (first error wins).
+cudaError_t read_device_status(int32_t* status, bool clear);
+
+}  // namespace smla

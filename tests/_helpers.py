@@ -1,0 +1,66 @@
+"""Shared test plumbing: building inputs on the GPU, running the oracle on host
+copies of the referenced rows, and the parity tolerances."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle.mla_oracle as O
+from sparse_mla_decode_03_gb300 import workloads as W
+
+SCALE = 1.0 / math.sqrt(512)
+
+# Parity bar: bf16 output within 1e-2 absolute plus one bf16 rounding step of the
+# reference (2^-8 relative; needed only where |out| >> 1, e.g. with x50 outliers),
+# fp32 LSE within 1e-3 absolute.
+OUT_ABS = 1e-2
+OUT_REL = 2.0 ** -8
+LSE_ABS = 1e-3
+
+
+def assert_out_close(gpu_out: np.ndarray, ref: np.ndarray, strict_abs: bool = True):
+    gpu_out = np.asarray(gpu_out, dtype=np.float64)
+    err = np.abs(gpu_out - ref)
+    assert np.all(np.isfinite(gpu_out)), "non-finite output"
+    bound = OUT_ABS + OUT_REL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"out mismatch at {np.argwhere(bad)[:5].tolist()}: max err {err.max():.3g}, "
+        f"worst ratio {(err / bound).max():.3g}")
+    if strict_abs:
+        assert err.max() <= OUT_ABS, f"max abs err {err.max():.3g} > {OUT_ABS}"
+
+
+def assert_lse_close(gpu_lse: np.ndarray, ref: np.ndarray):
+    gpu_lse = np.asarray(gpu_lse, dtype=np.float64)
+    both_inf = np.isneginf(gpu_lse) & np.isneginf(ref)
+    assert np.array_equal(np.isneginf(gpu_lse), np.isneginf(ref)), "-inf pattern differs"
+    d = np.abs(np.where(both_inf, 0.0, gpu_lse - np.where(both_inf, 0.0, ref)))
+    assert d.max() <= LSE_ABS, f"lse max abs err {d.max():.3g}"
+
+
+def oracle_decode(q: torch.Tensor, kv: torch.Tensor, indices: np.ndarray, scale=SCALE,
+                  queries=None):
+    """Oracle on host copies; `queries` restricts to a subset of batch rows."""
+    idx = np.asarray(indices)
+    qsel = q if queries is None else q[list(queries)]
+    isel = idx if queries is None else idx[list(queries)]
+    rows, remap = W.compact_rows(kv, isel)
+    return O.sparse_mla_decode(W.bf16_bits(qsel), rows, remap, scale)
+
+
+def oracle_split(q, kv, indices, num_splits, scale=SCALE):
+    rows, remap = W.compact_rows(kv, np.asarray(indices))
+    return O.split_partials(W.bf16_bits(q), rows, remap, scale, num_splits)
+
+
+def small_case(B, H, n_rows, k, seed, device="cuda", outliers=0.0, pad_byte=0, law="uniform"):
+    """Cache of B sequences x n_rows rows, q, and k unique indices per query."""
+    w = W.Workload(f"small{seed}", B, H, k, n_rows, law, outlier_frac=outliers, seed=seed)
+    L = W.seq_lengths(w)
+    kv = W.make_cache(w, L, device=device, pad_byte=pad_byte)
+    q = W.make_q(w, device=device)
+    idx = W.make_indices(w, L) if k <= n_rows else None
+    return w, kv, q, idx
