@@ -163,6 +163,29 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray,
     return out, lse
 
 
+def weighted_deviation(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray,
+                       scale: float) -> np.ndarray:
+    """D[b, h, c] = sum_t w_t |k_nope[t, c] - out[b, h, c]|, w_t = exp(s_t - lse).
+
+    Not part of the method: it sizes the forward error of any implementation that
+    rounds the attention weights to a p-bit format before the weighted sum.  With
+    each weight perturbed by a relative eps_t and renormalised, the output moves by
+    sum_t w_t eps_t (k_nope[t] - out), so |error| <= max|eps| * D to first order."""
+    q = bf16_bits_to_float(q_bits)
+    B, H, _ = q.shape
+    D = np.zeros((B, H, NOPE_DIM))
+    for b in range(B):
+        k_nope, k_rope = dequantize_rows(_valid_rows(kv, indices[b]))
+        if k_nope.shape[0] == 0:
+            continue
+        s = scale * (q[b, :, :NOPE_DIM] @ k_nope.T + q[b, :, NOPE_DIM:] @ k_rope.T)
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        out = w @ k_nope
+        D[b] = np.einsum("ht,htc->hc", w, np.abs(k_nope[None, :, :] - out[:, None, :]))
+    return D
+
+
 # ---------------------------------------------------------------------------
 # Split-K over the top-k positions, and the merge of partials
 # ---------------------------------------------------------------------------

@@ -12,19 +12,23 @@ from sparse_mla_decode_03_gb300 import workloads as W
 
 SCALE = 1.0 / math.sqrt(512)
 
-# Parity bar: bf16 output within 1e-2 absolute plus one bf16 rounding step of the
-# reference (2^-8 relative; needed only where |out| >> 1, e.g. with x50 outliers),
-# fp32 LSE within 1e-3 absolute.
+# Parity bar.  fp32 LSE within 1e-3 absolute.  bf16 output within 1e-2 absolute
+# everywhere the outputs are O(1) (strict_abs).  Where |out| >> 1 (the x50-outlier
+# workload) no bf16 result can be within 1e-2, so the bound adds the bf16 rounding
+# of the output (2^-8 |ref|) and of the attention weights that feed the bf16 PV
+# product (2^-8 D, D = sum_t w_t |v_t - ref|, see oracle.weighted_deviation).
 OUT_ABS = 1e-2
 OUT_REL = 2.0 ** -8
 LSE_ABS = 1e-3
 
 
-def assert_out_close(gpu_out: np.ndarray, ref: np.ndarray, strict_abs: bool = True):
+def assert_out_close(gpu_out: np.ndarray, ref: np.ndarray, strict_abs: bool = True, D=None):
     gpu_out = np.asarray(gpu_out, dtype=np.float64)
     err = np.abs(gpu_out - ref)
     assert np.all(np.isfinite(gpu_out)), "non-finite output"
     bound = OUT_ABS + OUT_REL * np.abs(ref)
+    if D is not None:
+        bound = bound + OUT_REL * D
     bad = err > bound
     assert not bad.any(), (
         f"out mismatch at {np.argwhere(bad)[:5].tolist()}: max err {err.max():.3g}, "
@@ -49,6 +53,14 @@ def oracle_decode(q: torch.Tensor, kv: torch.Tensor, indices: np.ndarray, scale=
     isel = idx if queries is None else idx[list(queries)]
     rows, remap = W.compact_rows(kv, isel)
     return O.sparse_mla_decode(W.bf16_bits(qsel), rows, remap, scale)
+
+
+def oracle_deviation(q, kv, indices, scale=SCALE, queries=None):
+    idx = np.asarray(indices)
+    qsel = q if queries is None else q[list(queries)]
+    isel = idx if queries is None else idx[list(queries)]
+    rows, remap = W.compact_rows(kv, isel)
+    return O.weighted_deviation(W.bf16_bits(qsel), rows, remap, scale)
 
 
 def oracle_split(q, kv, indices, num_splits, scale=SCALE):

@@ -235,6 +235,22 @@ def test_closed_form_two_rows_sigmoid():
         assert abs(lse[0, h] - (big + math.log(math.exp(s1 - big) + math.exp(s2 - big)))) < 1e-12
 
 
+def test_weighted_deviation_closed_forms():
+    """Two rows: D = 2 w1 w2 |v1 - v2|; identical rows: D = 0."""
+    w, kv, qbits, q = tiny_inputs(1, 2, 64, seed=3)
+    idx = np.array([[5, 40]])
+    D = O.weighted_deviation(qbits, kv, idx, SCALE)
+    nope, rope = O.dequantize_rows(kv[[5, 40]])
+    qf = q.to(torch.float64).numpy()[0]
+    for h in range(2):
+        s1 = _scores_by_hand(qf[h], nope[0], rope[0], SCALE)
+        s2 = _scores_by_hand(qf[h], nope[1], rope[1], SCALE)
+        a = 1.0 / (1.0 + math.exp(s2 - s1))
+        assert np.max(np.abs(D[0, h] - 2 * a * (1 - a) * np.abs(nope[0] - nope[1]))) < 1e-12
+    kv2 = np.repeat(kv[[3]], 20, axis=0)
+    assert np.all(O.weighted_deviation(qbits, kv2, np.arange(20)[None], SCALE) < 1e-12)
+
+
 def test_closed_form_zero_query_is_mean():
     w, kv, _, _ = tiny_inputs(1, 2, 100, seed=4)
     qbits = np.zeros((1, 2, 512), np.uint16)

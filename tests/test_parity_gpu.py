@@ -8,14 +8,14 @@ from sparse_mla_decode_03_gb300 import (sparse_mla_combine, sparse_mla_decode,
                                         sparse_mla_decode_split, smla_device_status)
 from sparse_mla_decode_03_gb300 import workloads as W
 
-from _helpers import (SCALE, assert_lse_close, assert_out_close, oracle_decode, oracle_split,
-                      small_case)
+from _helpers import (SCALE, assert_lse_close, assert_out_close, oracle_decode,
+                      oracle_deviation, oracle_split, small_case)
 
 pytestmark = pytest.mark.gpu
 
 
 def _run(q, kv, idx_np, **kw):
-    idx = torch.as_tensor(idx_np, dtype=torch.int32, device="cuda")
+    idx = torch.as_tensor(np.ascontiguousarray(idx_np), dtype=torch.int32, device="cuda")
     out, lse = sparse_mla_decode(q, kv, idx, **kw)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), lse.cpu().numpy()
@@ -95,7 +95,7 @@ def test_pad_byte_ff_and_outliers():
     w, kv, q, idx = small_case(2, 64, 1000, 512, seed=12, outliers=0.01, pad_byte=0xFF)
     out, lse = _run(q, kv, idx)
     ro, rl = oracle_decode(q, kv, idx)
-    assert_out_close(out, ro, strict_abs=False)
+    assert_out_close(out, ro, strict_abs=False, D=oracle_deviation(q, kv, idx))
     assert_lse_close(lse, rl)
 
 
@@ -164,7 +164,8 @@ def test_combine_matches_oracle(S):
     out, lse = sparse_mla_combine(o, l)
     torch.cuda.synchronize()
     ro, rl = O.combine(o.double().cpu().numpy(), l.double().cpu().numpy())
-    assert_out_close(out.float().cpu().numpy(), ro)
+    # random N(0,1) partials reach |o| ~ 4, where bf16's half-ulp alone is 0.0156
+    assert_out_close(out.float().cpu().numpy(), ro, strict_abs=False)
     assert_lse_close(lse.cpu().numpy(), rl)
 
 
@@ -182,7 +183,11 @@ def test_workload_parity(key):
     queries = range(w.batch) if w.batch <= 32 else range(0, w.batch, 3)
     ro, rl = oracle_decode(q, kv, idx, queries=queries)
     sel = list(queries)
-    assert_out_close(out[sel], ro, strict_abs=(w.outlier_frac == 0))
+    if w.outlier_frac == 0:
+        assert_out_close(out[sel], ro)
+    else:
+        D = oracle_deviation(q, kv, idx, queries=queries)
+        assert_out_close(out[sel], ro, strict_abs=False, D=D)
     assert_lse_close(lse[sel], rl)
     del kv
     torch.cuda.empty_cache()
