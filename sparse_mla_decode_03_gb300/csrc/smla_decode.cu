@@ -7,22 +7,37 @@
 //      Context: A Kernel Optimization Campaign": one KV read shared by all heads),
 //   2. dequantises the FP8 e4m3 nope part with its per-64-column UE8M0 scales into a
 //      bf16 tile ("The Power-of-Two Trap: Debugging a Triton MMA Kernel on Blackwell
-//      GPUs", section "3. The Scale Indexing Complication"), next to the bf16 rope,
+//      GPUs", section "3. The Scale Indexing Complication") next to the bf16 rope,
 //   3. computes S^T = K_tile . Q^T on the tensor cores (tcgen05.mma, M = 128 tokens,
 //      N = NH heads, K = 512) into tensor memory,
-//   4. runs the online softmax over the tile (running max / sum per head),
-//   5. accumulates O^T += V_tile^T . P^T on the tensor cores (M = 128 value columns per
-//      block, 4 blocks, N = NH, K = 128 tokens) in tensor memory,
+//   4. runs the online softmax of the tile,
+//   5. accumulates O^T += V_tile^T . P^T on the tensor cores (4 blocks of M = 128
+//      value columns, N = NH, K = 128 tokens) in tensor memory,
 // and finally writes the normalised partial O and its log-sum-exp for the split
 // (the split-K scheme of "The 80KB Mystery: Resolving Contradictory Evidence in
 // Triton Kernel Optimization", section "The Context: Optimizing Attention on
 // Blackwell").
 //
-// Tokens are the MMA's M dimension so that every MMA is a full 128-row tcgen05
-// instruction even with 16 heads.  The same bf16 tile serves as K (K-major view) for
-// the scores and as V^T (MN-major view) for the output; its 4th 128-column block
-// holds dims 384..511 whose last 64 (the rope) produce output rows that are never
-// stored, so the 448-wide value product needs no separate padding.
+// Design (sm_103a).  Tokens are the MMA's M dimension, so every MMA is a full
+// 128-row tcgen05 instruction even with 16 heads.  One bf16 tile in shared memory
+// serves as K (K-major view) for the scores and as V^T (MN-major view) for the
+// output.  The 448-wide value product runs as four 128-row blocks; the 4th block
+// pairs value columns 384..447 with a constant block whose first column is 1, so
+// output row 448 of that block is sum_t P[t], the softmax denominator, accumulated
+// and rescaled by the tensor core together with O.
+//
+// Warp roles (512 threads):
+//   warp 0       allocates tensor memory and issues every tcgen05.mma (one lane)
+//   warps 4..7   softmax and epilogue; thread t owns TMEM lane t (token t of the
+//                tile for S^T, value row t of each block for O^T)
+//   warps 8..15  loaders: read the next tile's rows into registers while the
+//                current tile computes, then dequantise into shared memory as
+//                soon as the tensor core has released each half of the tile
+//   warps 1..3   idle
+// Pipeline per tile i: loaders fill half A (columns 0..255) and half B (256..511)
+// -> QK(i) -> softmax(i) -> PV(i) blocks 0,1 release half A -> PV(i) blocks 2,3
+// release half B.  All waits are bounded; on timeout the CTA records
+// SMLA_ERR_TIMEOUT in the device status word and leaves through the epilogue.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,11 +51,18 @@ __device__ int g_smla_status = 0;
 
 namespace {
 
-constexpr int kTile = 128;                    // tokens per tile (MMA M)
-constexpr int kChunkBytes = kTile * 128;      // one 64-column bf16 slab of the tile
-constexpr int kThreads = 128;
+constexpr int kTile = 128;                      // tokens per tile (MMA M)
+constexpr int kChunkBytes = kTile * 128;        // one 64-column bf16 slab of the tile
+constexpr int kThreads = 512;
+constexpr int kLoaderWarp0 = 8;
+constexpr int kLoaderWarps = 8;
+constexpr int kSoftWarp0 = 4;
 constexpr long long kWaitLimit = 2000000000LL;  // ~1 s of SM clocks
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLazyMax = 8.0f;                // log2 headroom before the max is raised
+constexpr int kRowWords = 73;                   // 584 bytes = 73 x 8
+
+enum Bar : int { B_Q = 0, B_FULLA, B_FULLB, B_FREEA, B_FREEB, B_SFULL, B_PFULL, B_ODONE, B_COUNT };
 
 template <int NH>
 struct Cfg {
@@ -49,16 +71,18 @@ struct Cfg {
   static constexpr int kPOff = kQOff + 8 * kQChunk;
   static constexpr int kPRow = 2 * NH;
   static constexpr int kPBytes = kTile * kPRow;
-  static constexpr int kMiscOff = kPOff + ((kPBytes + 1023) / 1024) * 1024;
+  static constexpr int kOnesOff = kPOff + ((kPBytes + 1023) / 1024) * 1024;  // 2 KB, 1024-aligned
+  static constexpr int kMiscOff = kOnesOff + 2048;
   static constexpr int kRedOff = kMiscOff;                 // float [4][NH]
-  static constexpr int kMOff = kRedOff + 4 * NH * 4;       // float [2][NH] running max
-  static constexpr int kValidOff = kMOff + 2 * NH * 4;     // uint8 [128]
-  static constexpr int kBarOff = kValidOff + 128;          // uint64
-  static constexpr int kTaddrOff = kBarOff + 8;            // uint32
-  static constexpr int kFlagOff = kTaddrOff + 4;           // int
-  static constexpr int kSmemBytes = kFlagOff + 4 + 1024;   // + alignment slack
-  static constexpr uint32_t kTmemCols =
-      5 * NH <= 32 ? 32 : 5 * NH <= 64 ? 64 : 5 * NH <= 128 ? 128 : 5 * NH <= 256 ? 256 : 512;
+  static constexpr int kMOff = kRedOff + 4 * NH * 4;       // float [2][NH] running max (log2)
+  static constexpr int kLOff = kMOff + 2 * NH * 4;         // float [NH] final denominators
+  static constexpr int kBarOff = kLOff + NH * 4;           // uint64 [B_COUNT]
+  static constexpr int kTaddrOff = kBarOff + 8 * B_COUNT;  // uint32
+  static constexpr int kAbortOff = kTaddrOff + 4;          // int
+  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
+  // S^T (NH columns), O^T (4 x NH), per-thread fp32 softmax sums (NH)
+  static constexpr uint32_t kTmemCols = 6 * NH <= 64 ? 64 : 6 * NH <= 128 ? 128
+                                      : 6 * NH <= 256 ? 256 : 512;
   static constexpr uint32_t kPSwz = NH == 64 ? SWZ_128B : NH == 32 ? SWZ_64B : SWZ_32B;
 };
 
@@ -72,17 +96,36 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
 }
-
-__device__ __forceinline__ uint2 ldg_nc_u2(const uint2* p) {
+__device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
   return v;
 }
-
 __device__ __forceinline__ float warp_max(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
+}
+// Barrier among the 128 softmax threads (id 1); returns true if any thread passed true.
+__device__ __forceinline__ bool softmax_bar_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.or.pred b, 1, 128, a;\n\tselp.u32 %0, 1, 0, b;\n\t}\n"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 2^x on the SFU (ex2.approx, relative error ~2^-22; subnormal results flush to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // UE8M0 byte -> fp32 2^(e-127) (e = 0 is the fp32 subnormal 2^-127, 0xFF is NaN).
@@ -91,7 +134,10 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t e) {
   return __uint_as_float(bits);
 }
 
-// Two e4m3 bytes (low byte = first element) -> bf16x2 of value * scale.
+// Two e4m3 bytes (low byte = first element) -> bf16x2 of value * scale.  e4m3 ->
+// f16 is exact, f16 -> f32 is exact, the product by a power of two is exact unless
+// it leaves the fp32 range, and the final rounding to bf16 is exact whenever the
+// product is a normal bf16 (e4m3 has 3 mantissa bits).
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t two, float scale) {
   uint32_t h2;
   const uint16_t in = static_cast<uint16_t>(two);
@@ -101,8 +147,6 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t two, float scale) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
   return *reinterpret_cast<const uint32_t*>(&b);
 }
-
-// 8 e4m3 bytes -> 8 bf16 (16 bytes).
 __device__ __forceinline__ uint4 dequant8(uint2 w, float scale) {
   uint4 r;
   r.x = dequant_pair(w.x & 0xffffu, scale);
@@ -112,68 +156,196 @@ __device__ __forceinline__ uint4 dequant8(uint2 w, float scale) {
   return r;
 }
 
+// Fast path for scale bytes s <= 142.  e4m3 -> f16 is exact and every non-zero e4m3
+// value is a normal f16 whose low 7 mantissa bits are zero, so shifting the f16
+// exponent and mantissa right by 3 (sign kept) gives bf16 bits of value * 2^-112
+// exactly (zero stays zero).  Multiplying by the bf16 2^(s - 15) (exponent field
+// s + 112 <= 254) then gives value * 2^(s - 127), exact whenever the result is a
+// normal bf16.
+__device__ __forceinline__ uint32_t bf16x2_scale_bits(uint32_t s) {
+  const uint32_t e = (s + 112u) << 7;
+  return e | (e << 16);
+}
+__device__ __forceinline__ uint32_t dequant_pair_fast(uint32_t two, uint32_t mult2) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(two);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  const uint32_t y = ((h2 & 0x7fff7fffu) >> 3) | (h2 & 0x80008000u);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(mult2));
+  return r;
+}
+// 8 e4m3 bytes with scale byte s -> 8 bf16.
+__device__ __forceinline__ uint4 dequant8_s(uint2 w, uint32_t s) {
+  if (s <= 142u) {
+    const uint32_t m = bf16x2_scale_bits(s);
+    uint4 r;
+    r.x = dequant_pair_fast(w.x & 0xffffu, m);
+    r.y = dequant_pair_fast(w.x >> 16, m);
+    r.z = dequant_pair_fast(w.y & 0xffffu, m);
+    r.w = dequant_pair_fast(w.y >> 16, m);
+    return r;
+  }
+  return dequant8(w, ue8m0_to_f32(s));
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// Gathers and dequantises the 32 tile rows owned by this warp.  A row is 73 8-byte
-// words: words 0..55 nope, word 56 the 7 scales + pad, words 57..72 rope.  Lane l
-// loads words l, 32 + l and (l < 9) 64 + l, so each row is read with coalesced
-// 8-byte loads.  Rows that are masked, beyond the split or out of range are written
-// as zeros.
-template <int NH>
-__device__ __forceinline__ void gather_rows(uint32_t sbase, uint8_t* vflag, const uint8_t* kv,
-                                            const int32_t* idx_row, int tile0, int t_end,
-                                            int64_t num_rows, int64_t stride, int warp,
-                                            int lane) {
-  constexpr int kBatch = 4;
-  const uint2 zero = make_uint2(0u, 0u);
-#pragma unroll 1
-  for (int i0 = 0; i0 < 32; i0 += kBatch) {
-    uint2 wa[kBatch], wb[kBatch], wc[kBatch];
-    bool val[kBatch];
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int r = warp * 32 + i0 + j;
-      const int pos = tile0 + r;
-      int idx = -1;
-      if (pos < t_end) idx = __ldg(idx_row + pos);
-      bool v = idx >= 0;
-      if (v && static_cast<int64_t>(idx) >= num_rows) {
-        v = false;
-        if (lane == 0) record_status(SMLA_ERR_INDEX_RANGE);
-      }
-      val[j] = v;
-      const uint2* row =
-          reinterpret_cast<const uint2*>(kv + (v ? static_cast<int64_t>(idx) * stride : 0));
-      wa[j] = v ? ldg_nc_u2(row + lane) : zero;
-      wb[j] = v ? ldg_nc_u2(row + 32 + lane) : zero;
-      wc[j] = (v && lane < 9) ? ldg_nc_u2(row + 64 + lane) : zero;
+// Bounded mbarrier wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_f) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_f) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      *abort_f = 1;
+      record_status(SMLA_ERR_TIMEOUT);
+      return false;
     }
+  }
+  return true;
+}
+
+struct Split {
+  int t_begin, t_end, ntiles;
+};
+__device__ __forceinline__ Split split_range(int topk, int S, int s) {
+  const int G = (topk + 15) >> 4;
+  const int g0 = static_cast<int>((static_cast<int64_t>(s) * G) / S);
+  const int g1 = static_cast<int>((static_cast<int64_t>(s + 1) * G) / S);
+  Split r;
+  r.t_begin = min(16 * g0, topk);
+  r.t_end = min(16 * g1, topk);
+  r.ntiles = (r.t_end - r.t_begin + kTile - 1) / kTile;
+  return r;
+}
+
+// Row id of tile slot `pos`, or -1 if the slot is masked, past the split or out of
+// range (the latter is also reported).
+__device__ __forceinline__ int64_t slot_row(const int32_t* idx_row, int pos, int t_end,
+                                            int64_t num_rows, bool report) {
+  if (pos >= t_end) return -1;
+  const int idx = __ldg(idx_row + pos);
+  if (idx < 0) return -1;
+  if (static_cast<int64_t>(idx) >= num_rows) {
+    if (report) record_status(SMLA_ERR_INDEX_RANGE);
+    return -1;
+  }
+  return idx;
+}
+
+// ---------------------------------------------------------------------------
+// Loader: 8 warps, each owns 16 rows of the tile as 4 groups of 4 rows, 8 lanes per
+// row, so every load instruction reads 128 contiguous bytes of 4 rows.  A row
+// starting at byte address a (8-byte aligned) is read as 16-byte chunks from
+// a & ~15: lane q reads chunks q + 8j, j = 0..4 (37 chunks; the last is read as 8
+// bytes when the row is 16-byte aligned, so nothing past the row is touched).
+// With s = 1 for rows that start 8 bytes into a chunk, chunk c holds row words
+// 2c - s and 2c + 1 - s.  Word w < 56: nope columns 8w..8w+7 (scale group w / 8);
+// w = 56: the 7 scales and the pad; w = 57..72: rope.  Half A of the tile = words
+// 0..31, half B = words 32..72.
+// ---------------------------------------------------------------------------
+constexpr int kSlots = 5;
+
+struct RowRegs {
+  uint4 c[kSlots];
+  uint32_t s8;
+};
+
+__device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void load_row(RowRegs& R, const uint8_t* row, int q) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  if (row == nullptr) {
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const uint32_t r = static_cast<uint32_t>(warp * 32 + i0 + j);
-      const uint32_t sc_lo = __shfl_sync(0xffffffffu, wb[j].x, 24);
-      const uint32_t sc_hi = __shfl_sync(0xffffffffu, wb[j].y, 24);
-      // word `lane`: columns 8*lane.., group lane/8 (0..3)
-      const float fa = ue8m0_to_f32((sc_lo >> (8 * (lane >> 3))) & 0xffu);
-      st_shared_v4(sbase + (lane >> 3) * kChunkBytes + swz_offset(r, lane & 7, 128),
-                   dequant8(wa[j], fa));
-      if (lane < 24) {
-        // word 32 + lane: group 4 + lane/8 (4..6) = byte lane/8 of the high scale word
-        const float fb = ue8m0_to_f32((sc_hi >> (8 * (lane >> 3))) & 0xffu);
-        st_shared_v4(sbase + (4 + (lane >> 3)) * kChunkBytes + swz_offset(r, lane & 7, 128),
-                     dequant8(wb[j], fb));
-      } else if (lane >= 25) {
-        const uint32_t rr = lane - 25;  // rope word 0..6: rope columns 4rr..4rr+3
-        st_shared_v2(sbase + 7 * kChunkBytes + swz_offset(r, rr >> 1, 128) + (rr & 1) * 8, wb[j]);
+    for (int j = 0; j < kSlots; ++j) R.c[j] = z;
+    R.s8 = 0;
+    return;
+  }
+  const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
+  R.s8 = static_cast<uint32_t>((a >> 3) & 1);
+#pragma unroll
+  for (int j = 0; j < kSlots; ++j) {
+    const int c = q + 8 * j;
+    if (c < 36) {
+      R.c[j] = ldg_nc_u4(base + 16 * c);
+    } else if (c == 36) {
+      if (R.s8) {
+        R.c[j] = ldg_nc_u4(base + 16 * c);
+      } else {
+        const uint2 v = ldg_nc_u2(base + 16 * c);
+        R.c[j] = make_uint4(v.x, v.y, 0u, 0u);
       }
-      if (lane < 9) {
-        const uint32_t rr = 7 + lane;  // rope word 7..15
-        st_shared_v2(sbase + 7 * kChunkBytes + swz_offset(r, rr >> 1, 128) + (rr & 1) * 8, wc[j]);
-      }
-      if (lane == 0) vflag[r] = val[j] ? 1 : 0;
+    } else {
+      R.c[j] = z;
+    }
+  }
+}
+
+struct Scales {
+  uint32_t lo, hi;  // scale bytes of groups 0..3 and 4..6
+};
+
+__device__ __forceinline__ void nope_store(uint32_t tile, uint32_t r, int w, uint32_t x, uint32_t y,
+                                           const Scales& sc) {
+  const int g = w >> 3;
+  const uint32_t sb = g < 4 ? (sc.lo >> (8 * g)) & 0xffu : (sc.hi >> (8 * (g - 4))) & 0xffu;
+  st_shared_v4(tile + g * kChunkBytes + swz_offset(r, w & 7, 128), dequant8_s(make_uint2(x, y), sb));
+}
+__device__ __forceinline__ void rope_store(uint32_t tile, uint32_t r, int w, uint32_t x, uint32_t y) {
+  const uint32_t rr = static_cast<uint32_t>(w - 57);   // rope columns 4rr..4rr+3
+  st_shared_v2(tile + 7 * kChunkBytes + swz_offset(r, rr >> 1, 128) + (rr & 1) * 8,
+               make_uint2(x, y));
+}
+__device__ __forceinline__ void any_store(uint32_t tile, uint32_t r, int w, uint32_t x, uint32_t y,
+                                          const Scales& sc) {
+  if (w < 56) nope_store(tile, r, w, x, y, sc);
+  else if (w >= 57 && w < kRowWords) rope_store(tile, r, w, x, y);
+}
+
+// Stores half A (half == 0) or half B (half == 1) of one row into the bf16 tile.
+__device__ __forceinline__ void store_half(uint32_t tile, const RowRegs& R, uint32_t r, int q,
+                                           int lane, int half) {
+  const int s8 = static_cast<int>(R.s8);
+  // the scale word (w = 56) is in chunk 28 = slot 3 of lane 4 of this row
+  const uint32_t cand_lo = s8 ? R.c[3].z : R.c[3].x;
+  const uint32_t cand_hi = s8 ? R.c[3].w : R.c[3].y;
+  const int src = (lane & ~7) | 4;
+  Scales sc;
+  sc.lo = __shfl_sync(0xffffffffu, cand_lo, src);
+  sc.hi = __shfl_sync(0xffffffffu, cand_hi, src);
+  if (half == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {          // chunks 0..15: words -1..31
+      const int w0 = 2 * (q + 8 * j) - s8;
+      if (w0 >= 0) nope_store(tile, r, w0, R.c[j].x, R.c[j].y, sc);
+      nope_store(tile, r, w0 + 1, R.c[j].z, R.c[j].w, sc);
+    }
+    if (q == 0 && s8) nope_store(tile, r, 31, R.c[2].x, R.c[2].y, sc);   // chunk 16, low word
+  } else {
+    {                                      // chunks 16..23: words 31..47
+      const int w0 = 2 * (q + 16) - s8;
+      if (w0 >= 32) nope_store(tile, r, w0, R.c[2].x, R.c[2].y, sc);
+      nope_store(tile, r, w0 + 1, R.c[2].z, R.c[2].w, sc);
+    }
+    {                                      // chunks 24..31: words 47..63
+      const int w0 = 2 * (q + 24) - s8;
+      any_store(tile, r, w0, R.c[3].x, R.c[3].y, sc);
+      any_store(tile, r, w0 + 1, R.c[3].z, R.c[3].w, sc);
+    }
+    if (q <= 4) {                          // chunks 32..36: rope words 63..73
+      const int w0 = 2 * (q + 32) - s8;
+      rope_store(tile, r, w0, R.c[4].x, R.c[4].y);
+      if (w0 + 1 < kRowWords) rope_store(tile, r, w0 + 1, R.c[4].z, R.c[4].w);
     }
   }
 }
@@ -191,209 +363,344 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, h0 = blockIdx.y * NH, b = blockIdx.z;
-
-  const int G = (topk + 15) >> 4;
-  const int g0 = static_cast<int>((static_cast<int64_t>(s) * G) / S);
-  const int g1 = static_cast<int>((static_cast<int64_t>(s + 1) * G) / S);
-  const int t_begin = min(16 * g0, topk), t_end = min(16 * g1, topk);
-  const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
+  const Split sp = split_range(topk, S, s);
+  const int32_t* idx_row = indices + static_cast<int64_t>(b) * topk;
 
   float* red = reinterpret_cast<float*>(smem + C::kRedOff);
   float* mbuf = reinterpret_cast<float*>(smem + C::kMOff);
-  uint8_t* vflag = smem + C::kValidOff;
-  const uint32_t bar = sbase + C::kBarOff;
+  float* lfin = reinterpret_cast<float*>(smem + C::kLOff);
+  const uint32_t bars = sbase + C::kBarOff;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* taddr_s = reinterpret_cast<volatile uint32_t*>(smem + C::kTaddrOff);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(bar(B_Q), kLoaderWarps);
+    mbar_init(bar(B_FULLA), kLoaderWarps);
+    mbar_init(bar(B_FULLB), kLoaderWarps);
+    mbar_init(bar(B_FREEA), 1);
+    mbar_init(bar(B_FREEB), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_ODONE), 1);
+    *abort_f = 0;
     fence_mbar_init();
   }
-  if (tid < NH) mbuf[tid] = -INFINITY;
+  if (tid < 2 * NH) mbuf[tid] = -INFINITY;
   if (warp == 0) {
     tmem_alloc(sbase + C::kTaddrOff, C::kTmemCols);
     tmem_relinquish();
   }
-  // Q rows h0..h0+NH-1 of query b -> 8 K-major SW128 slabs of 64 columns.
-  for (int u = tid; u < NH * 64; u += kThreads) {
-    const int r = u >> 6, cu = u & 63;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-        q + (static_cast<int64_t>(b) * H + h0 + r) * kQkDim + cu * 8));
-    st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), v);
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *taddr_s;
   const uint32_t tS = tmem;        // S^T: columns [0, NH)
   const uint32_t tO = tmem + NH;   // O^T block mb: columns [NH + mb*NH, NH + (mb+1)*NH)
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tL = tmem + 5 * NH;  // this thread's partial sum_t P[t, h] in fp32
 
-  constexpr uint32_t kIdescQK = idesc_bf16(128, NH, false, false);
-  constexpr uint32_t kIdescPV = idesc_bf16(128, NH, true, true);
-
-  float l[NH];
+  // Registers: warpgroup 0 (MMA issuer + idle warps) gives up registers so that the
+  // softmax and loader warpgroups can hold a tile of raw rows and a row of scores.
+  // Each role runs entirely inside its own branch (no join before the end).
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    // ===================== MMA issuer =====================
+    if (warp == 0 && lane == 0 && sp.ntiles > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16(128, NH, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(128, NH, true, true);
+      bool ok = wait_or_abort(bar(B_Q), 0, abort_f);
+      // Base descriptors; moving a start address by X bytes adds X >> 4 to the low
+      // field (addresses stay below 256 KB, so the 14-bit field never carries).
+      const uint64_t dK = smem_desc(sbase, 16, 1024, SWZ_128B);
+      const uint64_t dQ = smem_desc(sbase + C::kQOff, 16, 1024, SWZ_128B);
+      const uint64_t dV = smem_desc(sbase, kChunkBytes, 1024, SWZ_128B);
+      // block 3 pairs columns 384..447 with the constant block: leading offset
+      // (ones - a_start) shrinks by 2048 bytes per K step
+      const uint64_t dV3 = smem_desc(sbase + 6 * kChunkBytes, C::kOnesOff - 6 * kChunkBytes, 1024,
+                                     SWZ_128B);
+      const uint64_t dP = smem_desc(sbase + C::kPOff, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
+      for (int it = 0; it < sp.ntiles && ok; ++it) {
+        const uint32_t par = it & 1;
+        ok = wait_or_abort(bar(B_FULLA), par, abort_f);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+          if (j == 4) {
+            ok = wait_or_abort(bar(B_FULLB), par, abort_f);
+            if (!ok) break;
+            tc_fence_after();
+          }
 #pragma unroll
-  for (int h = 0; h < NH; ++h) l[h] = 0.f;
-
-  uint32_t phase = 0;
-  bool failed = false;
-  const int32_t* idx_row = indices + static_cast<int64_t>(b) * topk;
-
-  for (int it = 0; it < ntiles; ++it) {
-    const int tile0 = t_begin + it * kTile;
-    gather_rows<NH>(sbase, vflag, kv, idx_row, tile0, t_end, num_rows, stride, warp, lane);
+          for (int k = 0; k < 4; ++k) {
+            mma_bf16_ss(tS, dK + static_cast<uint64_t>((j * kChunkBytes + k * 32) >> 4),
+                        dQ + static_cast<uint64_t>((j * C::kQChunk + k * 32) >> 4), kIdescQK,
+                        (j | k) != 0);
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(B_SFULL));
+        ok = wait_or_abort(bar(B_PFULL), par, abort_f);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = mb < 3
+                ? dV + static_cast<uint64_t>((2 * mb * kChunkBytes + ks * 2048) >> 4)
+                : dV3 + static_cast<uint64_t>(ks * 128) - (static_cast<uint64_t>(ks * 128) << 16);
+            mma_bf16_ss(tO + mb * NH, a, dP + static_cast<uint64_t>((ks * 16 * C::kPRow) >> 4),
+                        kIdescPV, (it > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (mb == 1) mma_commit(bar(B_FREEA));
+        }
+        mma_commit(bar(B_FREEB));
+      }
+      mma_commit(bar(B_ODONE));
+    }
+  } else if (warp >= kLoaderWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
+    // ===================== loaders =====================
+    const int lw = warp - kLoaderWarp0;          // 0..7
+    const int lt = tid - kLoaderWarp0 * 32;      // 0..255
+    const uint32_t tile = sbase;
+    // Q rows h0..h0+NH-1 -> 8 K-major SW128 slabs; the constant ones block.
+    for (int u = lt; u < NH * 64; u += kLoaderWarps * 32) {
+      const int r = u >> 6, cu = u & 63;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+          q + (static_cast<int64_t>(b) * H + h0 + r) * kQkDim + cu * 8));
+      st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), v);
+    }
+    if (lt < 128) {   // 16 rows x 8 units of 16 B
+      const uint32_t r = lt >> 3, unit = lt & 7;
+      const uint4 v = make_uint4(unit == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+      st_shared_v4(sbase + C::kOnesOff + (r >> 3) * 1024 + swz_offset(r & 7, unit, 128), v);
+    }
     fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(B_Q));
 
-    // ---- S^T = K . Q^T  (M = 128 tokens, N = NH, K = 512 in 32 steps) ----
-    if (tid == 0) {
+    const int q8 = lane & 7;                     // chunk lane within the row
+    const int rsub = lane >> 3;                  // row within a group of 4
+    RowRegs R[4];
+    int rows_next[4];
+    auto load_idx = [&](int it, int* out) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        out[g] = static_cast<int>(slot_row(idx_row, sp.t_begin + it * kTile + lw * 16 + 4 * g + rsub,
+                                           sp.t_end, num_rows, q8 == 0));
+    };
+    auto fetch = [&](const int* rows) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        load_row(R[g], rows[g] >= 0 ? kv + static_cast<int64_t>(rows[g]) * stride : nullptr, q8);
+    };
+    if (sp.ntiles > 0) {
+      int rows0[4];
+      load_idx(0, rows0);
+      fetch(rows0);
+      if (sp.ntiles > 1) load_idx(1, rows_next);
+    }
+    for (int it = 0; it < sp.ntiles; ++it) {
+      const uint32_t pprev = (it - 1) & 1;
+      if (it > 0 && !__all_sync(0xffffffffu, wait_or_abort(bar(B_FREEA), pprev, abort_f))) break;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) store_half(tile, R[g], lw * 16 + 4 * g + rsub, q8, lane, 0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_FULLA));
+      if (it > 0 && !__all_sync(0xffffffffu, wait_or_abort(bar(B_FREEB), pprev, abort_f))) break;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) store_half(tile, R[g], lw * 16 + 4 * g + rsub, q8, lane, 1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_FULLB));
+      if (it + 1 < sp.ntiles) {
+        fetch(rows_next);
+        if (it + 2 < sp.ntiles) load_idx(it + 2, rows_next);
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    // ===================== softmax + epilogue =====================
+    const int st = tid - kSoftWarp0 * 32;        // 0..127 = TMEM lane
+    const int sw = warp - kSoftWarp0;            // 0..3 = lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    int cur = 0;                                 // which half of mbuf holds the running max
+    bool ok = true;
+    // validity of this thread's token, read one tile ahead of its use
+    bool valid_next = sp.ntiles > 0 &&
+        slot_row(idx_row, sp.t_begin + st, sp.t_end, num_rows, false) >= 0;
+    for (int it = 0; it < sp.ntiles; ++it) {
+      const bool valid = valid_next;
+      if (it + 1 < sp.ntiles)
+        valid_next = slot_row(idx_row, sp.t_begin + (it + 1) * kTile + st, sp.t_end, num_rows,
+                              false) >= 0;
+      ok = wait_or_abort(bar(B_SFULL), it & 1, abort_f);
+      if (softmax_bar_or(!ok)) {   // leave together
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      float sv[NH];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int c = 0; c < NH / 16; ++c) tmem_ld16(tS + lane_base + 16 * c, sv + 16 * c);
+      tmem_wait_ld();
+      const float* m_old = mbuf + cur * NH;
+      float ex = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = smem_desc(sbase + j * kChunkBytes + k * 32, 16, 1024, SWZ_128B);
-          const uint64_t bq =
-              smem_desc(sbase + C::kQOff + j * C::kQChunk + k * 32, 16, 1024, SWZ_128B);
-          mma_bf16_ss(tS, a, bq, kIdescQK, (j | k) != 0);
+      for (int h4 = 0; h4 < NH / 4; ++h4) {
+        const float4 mo = reinterpret_cast<const float4*>(m_old)[h4];
+        const float mv[4] = {mo.x, mo.y, mo.z, mo.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 4 * h4 + i;
+          sv[h] = valid ? sv[h] * scale_log2 : -INFINITY;
+          ex = fmaxf(ex, sv[h] - mv[i]);   // -inf - m and NaN-free: sv = -inf only if invalid
         }
       }
-      mma_commit(bar);
-    }
-    bool ok = mbar_wait(bar, phase, kWaitLimit);
-    phase ^= 1u;
-    tc_fence_after();
-
-    float sv[NH];
+      if (!valid) ex = -INFINITY;
+      if (softmax_bar_or(ex > kLazyMax)) {
+        // Raise the running max to the exact tile max and rescale O (and with it
+        // the denominator row) by 2^(m_old - m_new).
 #pragma unroll
-    for (int c = 0; c < NH / 16; ++c) tmem_ld16(tS + lane_base + 16 * c, sv + 16 * c);
-    tmem_wait_ld();
-
-    // ---- online softmax (log2 domain) ----
-    const bool valid = vflag[tid] != 0;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) sv[h] = valid ? sv[h] * scale_log2 : -INFINITY;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const float m = warp_max(sv[h]);
-      if (lane == (h & 31)) red[warp * NH + h] = m;
-    }
-    __syncthreads();
-    const float* m_old = mbuf + (it & 1) * NH;
-    float* m_new_s = mbuf + ((it + 1) & 1) * NH;
-    bool rescale = false;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const float mt = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
-      const float mo = m_old[h];
-      const float mn = fmaxf(mo, mt);
-      const float alpha = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-      rescale |= alpha != 1.f;
-      const float p = (sv[h] == -INFINITY) ? 0.f : exp2f(sv[h] - mn);
-      l[h] = l[h] * alpha + p;
-      sv[h] = p;
-      if (tid == h) m_new_s[h] = mn;
-    }
-    // P^T row `tid` (NH bf16), MN-major with rows of 2*NH bytes
-#pragma unroll
-    for (int u = 0; u < NH / 8; ++u) {
-      uint4 v;
-      v.x = pack_bf16x2(sv[8 * u + 0], sv[8 * u + 1]);
-      v.y = pack_bf16x2(sv[8 * u + 2], sv[8 * u + 3]);
-      v.z = pack_bf16x2(sv[8 * u + 4], sv[8 * u + 5]);
-      v.w = pack_bf16x2(sv[8 * u + 6], sv[8 * u + 7]);
-      st_shared_v4(sbase + C::kPOff + swz_offset(tid, u, C::kPRow), v);
-    }
-    __syncthreads();  // m_new_s complete
-    if (rescale && it > 0) {
+        for (int h = 0; h < NH; ++h) {
+          const float m = warp_max(sv[h]);
+          if (lane == (h & 31)) red[sw * NH + h] = m;
+        }
+        softmax_bar();
+        float* m_new = mbuf + (cur ^ 1) * NH;
+        if (st < NH) {
+          const float mt = fmaxf(fmaxf(red[st], red[NH + st]), fmaxf(red[2 * NH + st], red[3 * NH + st]));
+          m_new[st] = fmaxf(m_old[st], mt);
+        }
+        softmax_bar();
+        if (it > 0) {
+          // 4 O^T blocks, then the fp32 partial sums (block 4 = tL)
 #pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb) {
+          for (int mb = 0; mb < 5; ++mb) {
 #pragma unroll
-        for (int c = 0; c < NH / 16; ++c) {
-          float o[16];
+            for (int c = 0; c < NH / 16; ++c) {
+              float o[16];
+              tmem_ld16(tO + lane_base + mb * NH + 16 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int h = 16 * c + i;
+                const float mn = m_new[h];
+                o[i] *= (mn == -INFINITY) ? 1.f : exp2f(m_old[h] - mn);
+              }
+              tmem_st16(tO + lane_base + mb * NH + 16 * c, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        cur ^= 1;
+      }
+      const float* m = mbuf + cur * NH;
+#pragma unroll
+      for (int h4 = 0; h4 < NH / 4; ++h4) {
+        const float4 mo = reinterpret_cast<const float4*>(m)[h4];
+        const float mv[4] = {mo.x, mo.y, mo.z, mo.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 4 * h4 + i;
+          // sv = -inf (masked) gives 0; m = -inf only while every score so far is
+          // masked, and then sv is -inf too
+          sv[h] = (sv[h] == -INFINITY) ? 0.f : fast_exp2(sv[h] - mv[i]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NH / 8; ++u) {
+        uint4 v;
+        v.x = pack_bf16x2(sv[8 * u + 0], sv[8 * u + 1]);
+        v.y = pack_bf16x2(sv[8 * u + 2], sv[8 * u + 3]);
+        v.z = pack_bf16x2(sv[8 * u + 4], sv[8 * u + 5]);
+        v.w = pack_bf16x2(sv[8 * u + 6], sv[8 * u + 7]);
+        st_shared_v4(sbase + C::kPOff + swz_offset(st, u, C::kPRow), v);
+      }
+      // unrounded sums for the log-sum-exp
+#pragma unroll
+      for (int c = 0; c < NH / 16; ++c) {
+        float lp[16];
+        if (it > 0) {
+          tmem_ld16(tL + lane_base + 16 * c, lp);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lp[i] += sv[16 * c + i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lp[i] = sv[16 * c + i];
+        }
+        tmem_st16(tL + lane_base + 16 * c, lp);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
+    }
+    // ---- epilogue ----
+    const bool have_o = !softmax_bar_or(
+        !(sp.ntiles > 0 && ok && wait_or_abort(bar(B_ODONE), 0, abort_f)));
+    if (have_o) tc_fence_after();
+    if (have_o && sw == 2) {
+      // row 448 of block 3 (TMEM lane 64, lane 0 of this warp) = sum_t P[t] per head
+#pragma unroll
+      for (int c = 0; c < NH / 16; ++c) {
+        float o[16];
+        tmem_ld16(tO + lane_base + 3 * NH + 16 * c, o);
+        tmem_wait_ld();
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lfin[16 * c + i] = o[i];
+        }
+      }
+    } else if (!have_o && st < NH) {
+      lfin[st] = 0.f;
+    }
+    // sum the per-thread fp32 partials over the 128 threads for the LSE
+    if (have_o) {
+#pragma unroll
+      for (int c = 0; c < NH / 16; ++c) {
+        float lp[16];
+        tmem_ld16(tL + lane_base + 16 * c, lp);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float v = lp[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == ((16 * c + i) & 31)) red[sw * NH + 16 * c + i] = v;
+        }
+      }
+    }
+    softmax_bar();
+    const float* m = mbuf + cur * NH;
+    if (st < NH) {
+      const float lt = have_o ? (red[st] + red[NH + st]) + (red[2 * NH + st] + red[3 * NH + st]) : 0.f;
+      const float lse = lt > 0.f ? (m[st] + log2f(lt)) * kLn2 : -INFINITY;
+      lse_part[(static_cast<int64_t>(b) * H + h0 + st) * S + s] = lse;
+    }
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+      const int d = mb * 128 + st;
+#pragma unroll
+      for (int c = 0; c < NH / 16; ++c) {
+        float o[16];
+        if (have_o) {
           tmem_ld16(tO + lane_base + mb * NH + 16 * c, o);
           tmem_wait_ld();
+        }
+        if (d < kNope) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int h = 16 * c + i;
-            const float mn = m_new_s[h];
-            o[i] *= (mn == -INFINITY) ? 1.f : exp2f(m_old[h] - mn);
+            const float lt = lfin[h];
+            const float val = (have_o && lt > 0.f) ? o[i] / lt : 0.f;
+            o_part[((static_cast<int64_t>(b) * H + h0 + h) * S + s) * kNope + d] = val;
           }
-          tmem_st16(tO + lane_base + mb * NH + 16 * c, o);
-        }
-      }
-      tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- O^T += V^T . P^T  (4 blocks of M = 128 columns, N = NH, K = 128 tokens) ----
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a =
-              smem_desc(sbase + (2 * mb) * kChunkBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-          // N = NH is a single swizzle atom wide, so the leading offset is unused;
-          // it is set equal to the stride offset to keep every address in bounds.
-          const uint64_t bp = smem_desc(sbase + C::kPOff + ks * 16 * C::kPRow, 8 * C::kPRow,
-                                        8 * C::kPRow, C::kPSwz);
-          mma_bf16_ss(tO + mb * NH, a, bp, kIdescPV, (it > 0 || ks > 0) ? 1u : 0u);
-        }
-      }
-      mma_commit(bar);
-    }
-    ok = mbar_wait(bar, phase, kWaitLimit) && ok;
-    phase ^= 1u;
-    tc_fence_after();
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      if (tid == 0) record_status(SMLA_ERR_TIMEOUT);
-      break;
-    }
-  }
-
-  // ---- epilogue: l over the 128 threads, lse, normalised O ----
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    float v = l[h];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == (h & 31)) red[warp * NH + h] = v;
-  }
-  __syncthreads();
-  const float* m_fin = mbuf + (ntiles & 1) * NH;
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    const float lt = red[h] + red[NH + h] + red[2 * NH + h] + red[3 * NH + h];
-    l[h] = (lt > 0.f && !failed) ? 1.f / lt : 0.f;
-    if (tid == h) {
-      const float lse = (lt > 0.f && !failed) ? (m_fin[h] + log2f(lt)) * kLn2 : -INFINITY;
-      lse_part[(static_cast<int64_t>(b) * H + h0 + h) * S + s] = lse;
-    }
-  }
-  const bool have_o = ntiles > 0 && !failed;
-#pragma unroll 1
-  for (int mb = 0; mb < 4; ++mb) {
-    const int d = mb * 128 + tid;
-#pragma unroll
-    for (int c = 0; c < NH / 16; ++c) {
-      float o[16];
-      if (have_o) {
-        tmem_ld16(tO + lane_base + mb * NH + 16 * c, o);
-        tmem_wait_ld();
-      }
-      if (d < kNope) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = 16 * c + i;
-          const float val = (have_o && l[h] > 0.f) ? o[i] * l[h] : 0.f;
-          o_part[((static_cast<int64_t>(b) * H + h0 + h) * S + s) * kNope + d] = val;
         }
       }
     }
