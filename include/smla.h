@@ -61,6 +61,8 @@ enum smla_status {
   SMLA_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed           */
   SMLA_ERR_TIMEOUT = -6,            /* device status: a bounded wait in a kernel ran out */
   SMLA_ERR_INDEX_RANGE = -7,        /* device status: an index >= num_rows was skipped */
+  SMLA_ERR_RANGE = -8,              /* device status: a q or dequantised KV value is
+                                       outside the f16 range of the tensor-core operands */
 };
 
 /* Problem description shared by the entry points. */

@@ -17,6 +17,7 @@ SMLA_ERR_UNSUPPORTED_DEVICE = -4
 SMLA_ERR_CUDA = -5
 SMLA_ERR_TIMEOUT = -6
 SMLA_ERR_INDEX_RANGE = -7
+SMLA_ERR_RANGE = -8
 
 EXPORTED = (
     "smla_default_num_splits",

@@ -210,6 +210,7 @@ const char* smla_status_string(int status) {
     case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA: CUDA runtime error";
     case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
     case SMLA_ERR_INDEX_RANGE: return "SMLA_ERR_INDEX_RANGE: an index >= num_rows was skipped";
+    case SMLA_ERR_RANGE: return "SMLA_ERR_RANGE: a q or KV value exceeds the f16 operand range";
     default: return "SMLA: unknown status";
   }
 }

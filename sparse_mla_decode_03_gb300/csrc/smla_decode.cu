@@ -5,9 +5,9 @@
 //   1. gathers the selected 584-byte rows once for all NH heads ("The Moment of
 //      Compilation: When a Triton Kernel Meets Its Constraints", section "The
 //      Context: A Kernel Optimization Campaign": one KV read shared by all heads),
-//   2. dequantises the FP8 e4m3 nope part with its per-64-column UE8M0 scales into a
-//      bf16 tile ("The Power-of-Two Trap: Debugging a Triton MMA Kernel on Blackwell
-//      GPUs", section "3. The Scale Indexing Complication") next to the bf16 rope,
+//   2. dequantises the FP8 e4m3 nope part with its per-64-column UE8M0 scales into an
+//      f16 tile ("The Power-of-Two Trap: Debugging a Triton MMA Kernel on Blackwell
+//      GPUs", section "3. The Scale Indexing Complication") next to the rope,
 //   3. computes S^T = K_tile . Q^T on the tensor cores (tcgen05.mma, M = 128 tokens,
 //      N = NH heads, K = 512) into tensor memory,
 //   4. runs the online softmax of the tile,
@@ -19,7 +19,12 @@
 // Blackwell").
 //
 // Design (sm_103a).  Tokens are the MMA's M dimension, so every MMA is a full
-// 128-row tcgen05 instruction even with 16 heads.  One bf16 tile in shared memory
+// 128-row tcgen05 instruction even with 16 heads.  The nope operands are f16 (fp32
+// accumulation): e4m3 -> f16 is one conversion and the power-of-two group scale
+// one f16x2 multiply, with no integer work per element, and the attention weights
+// P keep 11 significant bits.  Nope values must lie in the f16 range (the kernel
+// reports SMLA_ERR_RANGE otherwise).  The rope columns stay bf16 and are multiplied
+// by bf16 q into the same fp32 accumulator.  One tile in shared memory
 // serves as K (K-major view) for the scores and as V^T (MN-major view) for the
 // output.  The 448-wide value product runs as four 128-row blocks; the 4th block
 // pairs value columns 384..447 with a constant block whose first column is 1, so
@@ -52,7 +57,7 @@ __device__ int g_smla_status = 0;
 namespace {
 
 constexpr int kTile = 128;                      // tokens per tile (MMA M)
-constexpr int kChunkBytes = kTile * 128;        // one 64-column bf16 slab of the tile
+constexpr int kChunkBytes = kTile * 128;        // one 64-column f16 slab of the tile
 constexpr int kThreads = 512;
 constexpr int kLoaderWarp0 = 8;
 constexpr int kLoaderWarps = 8;
@@ -134,64 +139,70 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t e) {
   return __uint_as_float(bits);
 }
 
-// Two e4m3 bytes (low byte = first element) -> bf16x2 of value * scale.  e4m3 ->
-// f16 is exact, f16 -> f32 is exact, the product by a power of two is exact unless
-// it leaves the fp32 range, and the final rounding to bf16 is exact whenever the
-// product is a normal bf16 (e4m3 has 3 mantissa bits).
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t two, float scale) {
+// f16 2^(s - 127) in both halves: normal for s in [113, 142], subnormal for
+// [103, 112], 0 below (such values are below the f16 range).
+__device__ __forceinline__ uint32_t f16_pow2x2(uint32_t s) {
+  const uint32_t bits = (s >= 113u && s <= 142u) ? ((s - 112u) << 10)
+                        : ((s >= 103u && s < 113u) ? (1u << (s - 103u)) : 0u);
+  return bits | (bits << 16);
+}
+// Two e4m3 bytes -> f16x2 of value * 2^(s - 127): e4m3 -> f16 is exact and the
+// product by a power of two is exact while it stays a normal f16.
+__device__ __forceinline__ uint32_t dq_pair_f16(uint32_t two, uint32_t m2) {
   uint32_t h2;
   const uint16_t in = static_cast<uint16_t>(two);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-  const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
-  const float2 f = __half22float2(hh);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-__device__ __forceinline__ uint4 dequant8(uint2 w, float scale) {
-  uint4 r;
-  r.x = dequant_pair(w.x & 0xffffu, scale);
-  r.y = dequant_pair(w.x >> 16, scale);
-  r.z = dequant_pair(w.y & 0xffffu, scale);
-  r.w = dequant_pair(w.y >> 16, scale);
-  return r;
-}
-
-// Fast path for scale bytes s <= 142.  e4m3 -> f16 is exact and every non-zero e4m3
-// value is a normal f16 whose low 7 mantissa bits are zero, so shifting the f16
-// exponent and mantissa right by 3 (sign kept) gives bf16 bits of value * 2^-112
-// exactly (zero stays zero).  Multiplying by the bf16 2^(s - 15) (exponent field
-// s + 112 <= 254) then gives value * 2^(s - 127), exact whenever the result is a
-// normal bf16.
-__device__ __forceinline__ uint32_t bf16x2_scale_bits(uint32_t s) {
-  const uint32_t e = (s + 112u) << 7;
-  return e | (e << 16);
-}
-__device__ __forceinline__ uint32_t dequant_pair_fast(uint32_t two, uint32_t mult2) {
-  uint32_t h2;
-  const uint16_t in = static_cast<uint16_t>(two);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-  const uint32_t y = ((h2 & 0x7fff7fffu) >> 3) | (h2 & 0x80008000u);
   uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(mult2));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h2), "r"(m2));
   return r;
 }
-// 8 e4m3 bytes with scale byte s -> 8 bf16.
-__device__ __forceinline__ uint4 dequant8_s(uint2 w, uint32_t s) {
-  if (s <= 142u) {
-    const uint32_t m = bf16x2_scale_bits(s);
-    uint4 r;
-    r.x = dequant_pair_fast(w.x & 0xffffu, m);
-    r.y = dequant_pair_fast(w.x >> 16, m);
-    r.z = dequant_pair_fast(w.y & 0xffffu, m);
-    r.w = dequant_pair_fast(w.y >> 16, m);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ bool f16x2_has_inf_or_nan(uint32_t v) {
+  return ((v & 0x7c00u) == 0x7c00u) || ((v & 0x7c000000u) == 0x7c000000u);
+}
+// 8 e4m3 bytes with scale byte s -> 8 f16.  |e4m3| <= 448, so s <= 134 can never
+// leave the f16 range; larger scales take a checked path that reports values
+// beyond it (SMLA_ERR_RANGE).
+__device__ __forceinline__ uint4 dequant8_f16(uint2 w, uint32_t s) {
+  uint4 r;
+  if (s <= 134u) {
+    const uint32_t m = f16_pow2x2(s);
+    r.x = dq_pair_f16(w.x & 0xffffu, m);
+    r.y = dq_pair_f16(w.x >> 16, m);
+    r.z = dq_pair_f16(w.y & 0xffffu, m);
+    r.w = dq_pair_f16(w.y >> 16, m);
     return r;
   }
-  return dequant8(w, ue8m0_to_f32(s));
+  const float sc = ue8m0_to_f32(s);
+  const uint32_t in[4] = {w.x & 0xffffu, w.x >> 16, w.y & 0xffffu, w.y >> 16};
+  uint32_t o[4];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h2;
+    const uint16_t v = static_cast<uint16_t>(in[i]);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    o[i] = pack_f16x2(f.x * sc, f.y * sc);
+    bad |= f16x2_has_inf_or_nan(o[i]);
+  }
+  if (bad) record_status(SMLA_ERR_RANGE);
+  r.x = o[0];
+  r.y = o[1];
+  r.z = o[2];
+  r.w = o[3];
+  return r;
 }
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Four bf16 (rope) -> four f16 (exact for magnitudes in [2^-14, 65504]).
+__device__ __forceinline__ uint2 bf16x4_to_f16x4(uint2 v) {
+  return make_uint2(pack_f16x2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u)),
+                    pack_f16x2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)));
 }
+
 
 // Bounded mbarrier wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_f) {
@@ -251,7 +262,7 @@ constexpr int kSlots = 5;
 
 struct RowRegs {
   uint4 c[kSlots];
-  uint32_t s8;
+  uint32_t s8a, s8b;   // row alignment shift seen by the half-A / half-B slots
 };
 
 __device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
@@ -262,24 +273,27 @@ __device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
   return v;
 }
 
+// Loads slots [J0, J1) of a row (half A = slots 0, 1; half B = slots 2..4).
+template <int J0, int J1>
 __device__ __forceinline__ void load_row(RowRegs& R, const uint8_t* row, int q) {
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   if (row == nullptr) {
 #pragma unroll
-    for (int j = 0; j < kSlots; ++j) R.c[j] = z;
-    R.s8 = 0;
+    for (int j = J0; j < J1; ++j) R.c[j] = z;
+    if (J0 == 0) R.s8a = 0; else R.s8b = 0;
     return;
   }
   const uintptr_t a = reinterpret_cast<uintptr_t>(row);
   const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~static_cast<uintptr_t>(15));
-  R.s8 = static_cast<uint32_t>((a >> 3) & 1);
+  const uint32_t s8 = static_cast<uint32_t>((a >> 3) & 1);
+  if (J0 == 0) R.s8a = s8; else R.s8b = s8;
 #pragma unroll
-  for (int j = 0; j < kSlots; ++j) {
+  for (int j = J0; j < J1; ++j) {
     const int c = q + 8 * j;
     if (c < 36) {
       R.c[j] = ldg_nc_u4(base + 16 * c);
     } else if (c == 36) {
-      if (R.s8) {
+      if (s8) {
         R.c[j] = ldg_nc_u4(base + 16 * c);
       } else {
         const uint2 v = ldg_nc_u2(base + 16 * c);
@@ -292,15 +306,17 @@ __device__ __forceinline__ void load_row(RowRegs& R, const uint8_t* row, int q) 
 }
 
 struct Scales {
-  uint32_t lo, hi;  // scale bytes of groups 0..3 and 4..6
+  uint32_t lo, hi;  // scale bytes of groups 0..3 and 4..6 (byte 7 = pad)
 };
 
+// Slow path: one word of any scale byte (also masked rows, whose bytes are 0).
 __device__ __forceinline__ void nope_store(uint32_t tile, uint32_t r, int w, uint32_t x, uint32_t y,
                                            const Scales& sc) {
   const int g = w >> 3;
   const uint32_t sb = g < 4 ? (sc.lo >> (8 * g)) & 0xffu : (sc.hi >> (8 * (g - 4))) & 0xffu;
-  st_shared_v4(tile + g * kChunkBytes + swz_offset(r, w & 7, 128), dequant8_s(make_uint2(x, y), sb));
+  st_shared_v4(tile + g * kChunkBytes + swz_offset(r, w & 7, 128), dequant8_f16(make_uint2(x, y), sb));
 }
+// Rope words stay bf16 (the rope slab is multiplied by bf16 q on the tensor core).
 __device__ __forceinline__ void rope_store(uint32_t tile, uint32_t r, int w, uint32_t x, uint32_t y) {
   const uint32_t rr = static_cast<uint32_t>(w - 57);   // rope columns 4rr..4rr+3
   st_shared_v2(tile + 7 * kChunkBytes + swz_offset(r, rr >> 1, 128) + (rr & 1) * 8,
@@ -312,10 +328,53 @@ __device__ __forceinline__ void any_store(uint32_t tile, uint32_t r, int w, uint
   else if (w >= 57 && w < kRowWords) rope_store(tile, r, w, x, y);
 }
 
-// Stores half A (half == 0) or half B (half == 1) of one row into the bf16 tile.
+// True if the 7 scale bytes all lie in [113, 134]: then 2^(s - 127) is a normal f16
+// and no value can leave the f16 range, so the fast path is exact.  Bytes are
+// checked two at a time in 16-bit lanes: +121 carries into bit 8 iff a byte > 134,
+// +143 carries iff a byte >= 113.
+__device__ __forceinline__ bool scales_fast(uint32_t lo, uint32_t hi) {
+  const uint32_t e0 = lo & 0x00ff00ffu, o0 = (lo >> 8) & 0x00ff00ffu;
+  const uint32_t e1 = hi & 0x00ff00ffu, o1 = (hi >> 8) & 0x000000ffu;   // pad byte excluded
+  const uint32_t over = ((e0 + 0x00790079u) | (o0 + 0x00790079u) | (e1 + 0x00790079u) |
+                         (o1 + 0x00000079u)) & 0x01000100u;
+  const uint32_t ge = (e0 + 0x008f008fu) & (o0 + 0x008f008fu) & (e1 + 0x008f008fu) &
+                      ((o1 + 0x0000008fu) | 0x01000000u);
+  return over == 0u && (ge & 0x01000100u) == 0x01000100u;
+}
+// f16x2 multiplier 2^(s - 127) from byte k of t = s - 112 (bytewise), s in [113, 134]:
+// byte k goes to bits 8..15 of both halves, then << 2 puts it in the exponent field.
+template <int K>
+__device__ __forceinline__ uint32_t mult_from(uint32_t t) {
+  constexpr uint32_t kSel = (K << 12) | 0x0400u | (K << 4) | 0x4u;
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(t), "n"(kSel));
+  return r << 2;
+}
+__device__ __forceinline__ uint4 dq8_fast(uint32_t x, uint32_t y, uint32_t m) {
+  uint4 v;
+  v.x = dq_pair_f16(x & 0xffffu, m);
+  v.y = dq_pair_f16(x >> 16, m);
+  v.z = dq_pair_f16(y & 0xffffu, m);
+  v.w = dq_pair_f16(y >> 16, m);
+  return v;
+}
+__device__ __forceinline__ void sts128_off(uint32_t addr, int off, uint4 v) {
+  st_shared_v4(addr + static_cast<uint32_t>(off), v);
+}
+
+// Stores half A (half == 0) or half B (half == 1) of one row into the f16 tile.
+//
+// Lane q of a row holds chunks q + 8j.  With d = 2q - s (s = alignment shift), its
+// words are w = d + h + 16j (h = 0: low 8 bytes of the chunk, h = 1: high), so
+// for each h the column group is 2j + ((d + h) >> 3) and the 16-byte unit within
+// the 128-byte row is (d + h) & 7: one address base per h, plus 32 KB per j.  The
+// only irregular word is lane 0 of a row with s = 1, whose (j = 0, h = 0) slot is
+// the previous row's tail; it takes word 31 from chunk 16 instead.
 __device__ __forceinline__ void store_half(uint32_t tile, const RowRegs& R, uint32_t r, int q,
                                            int lane, int half) {
-  const int s8 = static_cast<int>(R.s8);
+  // Half A of a tile is converted while slots 2..4 already hold the same tile (they
+  // were refilled after the previous tile's half B), so s8a == s8b then.
+  const int s8 = static_cast<int>(half == 0 ? R.s8a : R.s8b);
   // the scale word (w = 56) is in chunk 28 = slot 3 of lane 4 of this row
   const uint32_t cand_lo = s8 ? R.c[3].z : R.c[3].x;
   const uint32_t cand_hi = s8 ? R.c[3].w : R.c[3].y;
@@ -323,6 +382,56 @@ __device__ __forceinline__ void store_half(uint32_t tile, const RowRegs& R, uint
   Scales sc;
   sc.lo = __shfl_sync(0xffffffffu, cand_lo, src);
   sc.hi = __shfl_sync(0xffffffffu, cand_hi, src);
+  const bool masked = (sc.lo | (sc.hi & 0x00ffffffu)) == 0u;   // a zero-filled row
+  const int d = 2 * q - s8;
+  if (masked || scales_fast(sc.lo, sc.hi)) {
+    const uint32_t tlo = masked ? 0u : sc.lo - 0x70707070u;
+    const uint32_t thi = masked ? 0u : sc.hi - 0x00707070u;
+    const uint32_t rowbase = tile + r * 128u, rx = r & 7u;
+    const int b0 = d >> 3, b1 = (d + 1) >> 3;                     // -1, 0 or 1
+    const uint32_t base0 = rowbase + static_cast<uint32_t>(b0 * kChunkBytes) +
+                           ((static_cast<uint32_t>(d & 7) ^ rx) << 4);
+    const uint32_t base1 = rowbase + static_cast<uint32_t>(b1 * kChunkBytes) +
+                           ((static_cast<uint32_t>((d + 1) & 7) ^ rx) << 4);
+    if (half == 0) {
+      const uint32_t m0 = mult_from<0>(tlo), m1 = mult_from<1>(tlo);
+      const uint32_t m2 = mult_from<2>(tlo), m3 = mult_from<3>(tlo);
+      const bool tail = d < 0;                                      // lane 0, s = 1
+      // j = 0
+      {
+        const uint32_t x = tail ? R.c[2].x : R.c[0].x, y = tail ? R.c[2].y : R.c[0].y;
+        const uint32_t m = tail ? m3 : (b0 ? m1 : m0);
+        sts128_off(base0, tail ? 4 * kChunkBytes : 0, dq8_fast(x, y, m));
+        sts128_off(base1, 0, dq8_fast(R.c[0].z, R.c[0].w, b1 ? m1 : m0));
+      }
+      // j = 1
+      sts128_off(base0, 2 * kChunkBytes, dq8_fast(R.c[1].x, R.c[1].y, b0 < 0 ? m1 : (b0 ? m3 : m2)));
+      sts128_off(base1, 2 * kChunkBytes, dq8_fast(R.c[1].z, R.c[1].w, b1 ? m3 : m2));
+    } else {
+      const uint32_t m4 = mult_from<0>(thi), m5 = mult_from<1>(thi), m6 = mult_from<2>(thi);
+      const uint32_t m3 = mult_from<3>(tlo);
+      // j = 2: words 31..47 (word 31, the tail lane's, belongs to half A)
+      if (d >= 0) sts128_off(base0, 4 * kChunkBytes, dq8_fast(R.c[2].x, R.c[2].y, b0 ? m5 : m4));
+      sts128_off(base1, 4 * kChunkBytes, dq8_fast(R.c[2].z, R.c[2].w, b1 ? m5 : m4));
+      // j = 3: words 47..63: nope while group 2j + b <= 6, then the scale word, then rope
+      {
+        const int w0 = d + 48, w1 = d + 49;
+        if (w0 < 56) sts128_off(base0, 6 * kChunkBytes, dq8_fast(R.c[3].x, R.c[3].y, b0 < 0 ? m5 : m6));
+        else if (w0 >= 57) rope_store(tile, r, w0, R.c[3].x, R.c[3].y);
+        if (w1 < 56) sts128_off(base1, 6 * kChunkBytes, dq8_fast(R.c[3].z, R.c[3].w, m6));
+        else if (w1 >= 57) rope_store(tile, r, w1, R.c[3].z, R.c[3].w);
+      }
+      // j = 4: rope words 63..73
+      if (q <= 4) {
+        const int w0 = d + 64;
+        rope_store(tile, r, w0, R.c[4].x, R.c[4].y);
+        if (w0 + 1 < kRowWords) rope_store(tile, r, w0 + 1, R.c[4].z, R.c[4].w);
+      }
+      (void)m3;
+    }
+    return;
+  }
+  // Slow path: a scale byte outside [113, 134] somewhere in the row.
   if (half == 0) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {          // chunks 0..15: words -1..31
@@ -406,8 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     // ===================== MMA issuer =====================
     if (warp == 0 && lane == 0 && sp.ntiles > 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(128, NH, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(128, NH, true, true);
+      constexpr uint32_t kIdescQK = idesc_f16(128, NH, false, false);
+      constexpr uint32_t kIdescQKRope = idesc_bf16(128, NH, false, false);
+      constexpr uint32_t kIdescPV = idesc_f16(128, NH, true, true);
       bool ok = wait_or_abort(bar(B_Q), 0, abort_f);
       // Base descriptors; moving a start address by X bytes adds X >> 4 to the low
       // field (addresses stay below 256 KB, so the 14-bit field never carries).
@@ -433,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            mma_bf16_ss(tS, dK + static_cast<uint64_t>((j * kChunkBytes + k * 32) >> 4),
-                        dQ + static_cast<uint64_t>((j * C::kQChunk + k * 32) >> 4), kIdescQK,
-                        (j | k) != 0);
+            mma_f16_ss(tS, dK + static_cast<uint64_t>((j * kChunkBytes + k * 32) >> 4),
+                       dQ + static_cast<uint64_t>((j * C::kQChunk + k * 32) >> 4),
+                       j == 7 ? kIdescQKRope : kIdescQK, (j | k) != 0);
           }
         }
         if (!ok) break;
@@ -450,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a = mb < 3
                 ? dV + static_cast<uint64_t>((2 * mb * kChunkBytes + ks * 2048) >> 4)
                 : dV3 + static_cast<uint64_t>(ks * 128) - (static_cast<uint64_t>(ks * 128) << 16);
-            mma_bf16_ss(tO + mb * NH, a, dP + static_cast<uint64_t>((ks * 16 * C::kPRow) >> 4),
+            mma_f16_ss(tO + mb * NH, a, dP + static_cast<uint64_t>((ks * 16 * C::kPRow) >> 4),
                         kIdescPV, (it > 0 || ks > 0) ? 1u : 0u);
           }
           if (mb == 1) mma_commit(bar(B_FREEA));
@@ -466,15 +576,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lt = tid - kLoaderWarp0 * 32;      // 0..255
     const uint32_t tile = sbase;
     // Q rows h0..h0+NH-1 -> 8 K-major SW128 slabs; the constant ones block.
+    bool q_bad = false;
     for (int u = lt; u < NH * 64; u += kLoaderWarps * 32) {
       const int r = u >> 6, cu = u & 63;
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(
           q + (static_cast<int64_t>(b) * H + h0 + r) * kQkDim + cu * 8));
-      st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), v);
+      uint4 o = v;                       // the rope columns (slab 7) stay bf16
+      if (cu < 56) {
+        const uint2 lo = bf16x4_to_f16x4(make_uint2(v.x, v.y));
+        const uint2 hi = bf16x4_to_f16x4(make_uint2(v.z, v.w));
+        q_bad |= f16x2_has_inf_or_nan(lo.x) | f16x2_has_inf_or_nan(lo.y) |
+                 f16x2_has_inf_or_nan(hi.x) | f16x2_has_inf_or_nan(hi.y);
+        o = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      }
+      st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), o);
     }
+    if (q_bad) record_status(SMLA_ERR_RANGE);
     if (lt < 128) {   // 16 rows x 8 units of 16 B
       const uint32_t r = lt >> 3, unit = lt & 7;
-      const uint4 v = make_uint4(unit == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+      const uint4 v = make_uint4(unit == 0 ? 0x3C00u : 0u, 0u, 0u, 0u);   // f16 1.0
       st_shared_v4(sbase + C::kOnesOff + (r >> 3) * 1024 + swz_offset(r & 7, unit, 128), v);
     }
     fence_proxy_async_smem();
@@ -491,15 +611,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         out[g] = static_cast<int>(slot_row(idx_row, sp.t_begin + it * kTile + lw * 16 + 4 * g + rsub,
                                            sp.t_end, num_rows, q8 == 0));
     };
-    auto fetch = [&](const int* rows) {
+    // Half A (slots 0, 1) and half B (slots 2..4) of the staged rows are refilled
+    // separately, each right after it has been converted, so the loads for the
+    // next tile are in flight for a whole tile period.
+    auto fetch_a = [&](const int* rows) {
 #pragma unroll
       for (int g = 0; g < 4; ++g)
-        load_row(R[g], rows[g] >= 0 ? kv + static_cast<int64_t>(rows[g]) * stride : nullptr, q8);
+        load_row<0, 2>(R[g], rows[g] >= 0 ? kv + static_cast<int64_t>(rows[g]) * stride : nullptr, q8);
+    };
+    auto fetch_b = [&](const int* rows) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        load_row<2, kSlots>(R[g], rows[g] >= 0 ? kv + static_cast<int64_t>(rows[g]) * stride : nullptr,
+                            q8);
     };
     if (sp.ntiles > 0) {
       int rows0[4];
       load_idx(0, rows0);
-      fetch(rows0);
+      fetch_a(rows0);
+      fetch_b(rows0);
       if (sp.ntiles > 1) load_idx(1, rows_next);
     }
     for (int it = 0; it < sp.ntiles; ++it) {
@@ -510,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_FULLA));
+      if (it + 1 < sp.ntiles) fetch_a(rows_next);
       if (it > 0 && !__all_sync(0xffffffffu, wait_or_abort(bar(B_FREEB), pprev, abort_f))) break;
 #pragma unroll
       for (int g = 0; g < 4; ++g) store_half(tile, R[g], lw * 16 + 4 * g + rsub, q8, lane, 1);
@@ -517,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_FULLB));
       if (it + 1 < sp.ntiles) {
-        fetch(rows_next);
+        fetch_b(rows_next);
         if (it + 2 < sp.ntiles) load_idx(it + 2, rows_next);
       }
     }
@@ -614,10 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < NH / 8; ++u) {
         uint4 v;
-        v.x = pack_bf16x2(sv[8 * u + 0], sv[8 * u + 1]);
-        v.y = pack_bf16x2(sv[8 * u + 2], sv[8 * u + 3]);
-        v.z = pack_bf16x2(sv[8 * u + 4], sv[8 * u + 5]);
-        v.w = pack_bf16x2(sv[8 * u + 6], sv[8 * u + 7]);
+        v.x = pack_f16x2(sv[8 * u + 0], sv[8 * u + 1]);
+        v.y = pack_f16x2(sv[8 * u + 2], sv[8 * u + 3]);
+        v.z = pack_f16x2(sv[8 * u + 4], sv[8 * u + 5]);
+        v.w = pack_f16x2(sv[8 * u + 6], sv[8 * u + 7]);
         st_shared_v4(sbase + C::kPOff + swz_offset(st, u, C::kPRow), v);
       }
       // unrounded sums for the log-sum-exp
