@@ -189,6 +189,21 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
+def aggregate_over_ranks(ms_values, device, world_size):
+    """Max over ranks of each per-rank time (ms); identity when world_size == 1."""
+    if world_size == 1:
+        return list(ms_values)
+    import torch.distributed as dist
+    t = torch.tensor(list(ms_values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world_size, batch, ms_per_step):
+    """Whole-job queries/s: every rank decodes its own batch in ms_per_step (the max)."""
+    return world_size * batch / (ms_per_step * 1e-3)
+
+
 def config_dict(w, S):
     return {"workload": w.name, "batch": w.batch, "heads": w.heads, "topk": w.topk,
             "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
@@ -290,12 +305,9 @@ def run_gpu(args):
     d2h = out.numel() * out.element_size() + lse.numel() * 4
 
     # ---- aggregate over ranks ----
-    if ws > 1:
-        t = torch.tensor([ms, split_mean, e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, split_mean, e2e_ms = t.tolist()
-    value = ws * B / (ms * 1e-3)
-    e2e_value = ws * B / (e2e_ms * 1e-3)
+    ms, split_mean, e2e_ms = aggregate_over_ranks([ms, split_mean, e2e_ms], dev, ws)
+    value = job_throughput(ws, B, ms)
+    e2e_value = job_throughput(ws, B, e2e_ms)
 
     hbm_peak, tc_peak, peak_kind = read_peaks()
     mean_valid_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
