@@ -63,6 +63,8 @@ enum smla_status {
   SMLA_ERR_INDEX_RANGE = -7,        /* device status: an index >= num_rows was skipped */
   SMLA_ERR_RANGE = -8,              /* device status: a q or dequantised KV value is
                                        outside the f16 range of the tensor-core operands */
+  SMLA_ERR_SCRATCH_TOO_SMALL = -9,  /* sparse_mla_decode_noalloc: the split partials need
+                                       more than its built-in 16 MiB scratch */
 };
 
 /* Problem description shared by the entry points. */
@@ -122,6 +124,35 @@ int sparse_mla_decode_split(const void* q, const void* kv_cache, const int32_t* 
 int sparse_mla_combine(const float* o_part, const float* lse_part, int32_t batch,
                        int32_t num_heads, int32_t num_splits, void* out, float* lse,
                        smla_stream_t stream);
+
+/*
+ * sparse_mla_decode without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory: for example code that runs inside another framework's memory
+ * pool or a serving loop that must never call cudaMalloc (it can synchronise the
+ * device and fail under memory pressure).  Such a caller still owns q, kv_cache,
+ * indices, out and lse; only the split partials move into a scratch array that the
+ * library itself holds: 16 MiB of device memory in every GPU process that loads the
+ * library, kept until the process exits.  The function allocates nothing and calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *   - Same arguments and results as sparse_mla_decode, minus the workspace.
+ *   - num_splits = 0 takes the default plan, or the largest smaller split count
+ *     whose partials (smla_workspace_size bytes) fit in the scratch; an explicit
+ *     num_splits whose partials do not fit, or a problem for which even one split
+ *     does not fit (batch * num_heads above about 9300), returns
+ *     SMLA_ERR_SCRATCH_TOO_SMALL before anything is launched.
+ *   - The first call on each device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture on the device.
+ *   - All calls in the process share the one scratch array, which keeps the last
+ *     call's partials (every partial a call reads is written by the same call, so
+ *     nothing needs clearing).  Calls whose kernels overlap on the GPU (several
+ *     streams, or several host threads) race on it and must be serialised by the
+ *     caller.
+ */
+int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t* indices,
+                              void* out, float* lse, const smla_params* p, int32_t num_splits,
+                              smla_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* smla_status_string(int status);

@@ -18,6 +18,7 @@ SMLA_ERR_CUDA = -5
 SMLA_ERR_TIMEOUT = -6
 SMLA_ERR_INDEX_RANGE = -7
 SMLA_ERR_RANGE = -8
+SMLA_ERR_SCRATCH_TOO_SMALL = -9
 
 EXPORTED = (
     "smla_default_num_splits",
@@ -25,6 +26,7 @@ EXPORTED = (
     "sparse_mla_decode",
     "sparse_mla_decode_split",
     "sparse_mla_combine",
+    "sparse_mla_decode_noalloc",
     "smla_status_string",
     "smla_device_status",
 )
@@ -60,6 +62,7 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_decode.argtypes = [vp, vp, vp, vp, vp, P, i32, vp, sz, vp]
     lib.sparse_mla_decode_split.argtypes = [vp, vp, vp, P, i32, vp, vp, vp]
     lib.sparse_mla_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.sparse_mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, i32, vp]
     lib.smla_status_string.argtypes = [ctypes.c_int]
     lib.smla_status_string.restype = ctypes.c_char_p
     lib.smla_device_status.argtypes = [ctypes.POINTER(i32), i32]

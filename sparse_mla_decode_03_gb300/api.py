@@ -147,6 +147,27 @@ def sparse_mla_combine(o_part: torch.Tensor, lse_part: torch.Tensor,
     return out, lse
 
 
+def sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                              softmax_scale: float = DEFAULT_SCALE,
+                              out: Optional[torch.Tensor] = None,
+                              lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                              stream: Optional[torch.cuda.Stream] = None
+                              ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Whole decode step with the split partials in the library's built-in scratch
+    (no workspace argument; the C function allocates nothing).  Pass `out` and `lse`
+    to keep the call itself free of allocations."""
+    p = _params_from(q, kv_cache, indices, softmax_scale)
+    if out is None:
+        out = torch.empty((p.batch, p.num_heads, NOPE), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_heads), dtype=torch.float32, device=q.device)
+    st = _lib.load().sparse_mla_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(out),
+                                               _ptr(lse), ctypes.byref(p), num_splits,
+                                               _stream(stream))
+    _check(st, "sparse_mla_decode_noalloc")
+    return out, lse
+
+
 def smla_device_status(clear: bool = False) -> int:
     """Device status word (0, SMLA_ERR_TIMEOUT or SMLA_ERR_INDEX_RANGE); synchronises."""
     lib = _lib.load()

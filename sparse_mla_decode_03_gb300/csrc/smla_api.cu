@@ -211,6 +211,8 @@ const char* smla_status_string(int status) {
     case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
     case SMLA_ERR_INDEX_RANGE: return "SMLA_ERR_INDEX_RANGE: an index >= num_rows was skipped";
     case SMLA_ERR_RANGE: return "SMLA_ERR_RANGE: a q or KV value exceeds the f16 operand range";
+    case SMLA_ERR_SCRATCH_TOO_SMALL:
+      return "SMLA_ERR_SCRATCH_TOO_SMALL: split partials exceed the 16 MiB built-in scratch";
     default: return "SMLA: unknown status";
   }
 }

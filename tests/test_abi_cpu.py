@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-7, 1):
+    for code in range(-9, 1):
         s = lib.smla_status_string(code).decode()
         assert s.startswith("SMLA")
     assert "unknown" in lib.smla_status_string(-99).decode()
