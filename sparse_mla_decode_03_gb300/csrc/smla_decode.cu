@@ -75,9 +75,11 @@ constexpr float kLazyMax = 8.0f;                // log2 headroom before the max 
 
 // mbarriers.  FR: rope slab written; F0..F3: slab pairs (0,1), (2,3), (4,5) and slab
 // 6 written; E0..E3: value block 0..3 done (its slabs may be overwritten); SFULL:
-// scores in TMEM; PFULL: P in shared memory; ODONE: all value products done.
+// scores in TMEM; PFULL: P in shared memory; ODONE: all value products done; QRAW:
+// the bf16 q rows copied into the (not yet used) tile area.
 enum Bar : int {
-  B_FR = 0, B_F0, B_F1, B_F2, B_F3, B_E0, B_E1, B_E2, B_E3, B_SFULL, B_PFULL, B_ODONE, B_COUNT
+  B_FR = 0, B_F0, B_F1, B_F2, B_F3, B_E0, B_E1, B_E2, B_E3, B_SFULL, B_PFULL, B_ODONE, B_QRAW,
+  B_COUNT
 };
 
 template <int NH>
@@ -116,6 +118,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
 }
@@ -150,6 +160,17 @@ __device__ __forceinline__ bool workers_bar_or(bool p) {
   return r != 0;
 }
 __device__ __forceinline__ void workers_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// Barrier among the 512 workers; returns true if every thread passed true.
+__device__ __forceinline__ bool workers_bar_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 512, a;\n\tselp.u32 %0, 1, 0, b;\n\t}\n"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
 
 // 2^x on the SFU (ex2.approx, relative error ~2^-22; subnormal results flush to 0).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -299,6 +320,17 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return true;
 }
 
+// Wait of all 512 workers on an mbarrier phase: one thread polls it (bounded), the
+// others sleep on a named barrier, so the waiting warps take no issue slots and no
+// shared-memory bandwidth from the tensor core.  Every thread gets the same verdict.
+__device__ __forceinline__ bool workers_wait(uint32_t bar, uint32_t parity, volatile int* abort_f,
+                                             bool poller) {
+  bool ok = true;
+  if (poller) ok = wait_or_abort(bar, parity, abort_f);
+  __syncwarp();
+  return workers_bar_and(ok);
+}
+
 struct Split {
   int t_begin, t_end, ntiles;
 };
@@ -313,18 +345,19 @@ __device__ __forceinline__ Split split_range(int topk, int S, int s) {
   return r;
 }
 
-// Row id of tile slot `pos`, or -1 if the slot is masked, past the split or out of
-// range (the latter is also reported).
-__device__ __forceinline__ int slot_row(const int32_t* idx_row, int pos, int t_end,
-                                        int64_t num_rows, bool report) {
-  if (pos >= t_end) return -1;
-  const int idx = __ldg(idx_row + pos);
-  if (idx < 0) return -1;
+// Index of slot `pos` as stored (-1 past the split).  Loaded a tile ahead of its
+// use; nothing waits for it until then.
+__device__ __forceinline__ int raw_idx(const int32_t* idx_row, int pos, int t_end) {
+  return pos < t_end ? __ldg(idx_row + pos) : -1;
+}
+// A stored index names a row (out-of-range ones are masked and reported).
+__device__ __forceinline__ bool idx_ok(int idx, int64_t num_rows, bool report) {
+  if (idx < 0) return false;
   if (static_cast<int64_t>(idx) >= num_rows) {
     if (report) record_status(SMLA_ERR_INDEX_RANGE);
-    return -1;
+    return false;
   }
-  return idx;
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -429,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PFULL), kWorkerWarps);
     mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_QRAW), 1);
     *abort_f = 0;
     fence_mbar_init();
   }
@@ -448,11 +482,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsWg0) : "memory");
     // ===================== MMA issuer =====================
     if (warp == 0 && lane == 0 && sp.ntiles > 0) {
+      // The bf16 q rows h0..h0+NH-1 (contiguous, NH KB) into the still unused tile
+      // area, where the workers convert them into the Q operand.
+      {
+        const uint8_t* src =
+            reinterpret_cast<const uint8_t*>(q + (static_cast<int64_t>(b) * H + h0) * kQkDim);
+        mbar_arrive_expect_tx(bar(B_QRAW), NH * 1024);
+#pragma unroll
+        for (int k = 0; k < NH / 16; ++k)
+          bulk_g2s(sbase + k * 16384, src + k * 16384, 16384, bar(B_QRAW));
+      }
       constexpr uint32_t kIdescQK = idesc_f16(128, NH, false, false);
       constexpr uint32_t kIdescQKRope = idesc_bf16(128, NH, false, false);
       constexpr uint32_t kIdescPV = idesc_f16(128, NH, true, true);
-      // Base descriptors; moving a start address by X bytes adds X >> 4 to the low
-      // field (addresses stay below 256 KB, so the 14-bit field never carries).
+      // Descriptors as 32-bit halves: moving a start address by X bytes adds X >> 4 to
+      // the low half (addresses stay below 256 KB, so the 14-bit field never
+      // carries); the high halves (stride, swizzle) are fixed.
       const uint64_t dK = smem_desc(sbase, 16, 1024, SWZ_128B);
       const uint64_t dQ = smem_desc(sbase + C::kQOff, 16, 1024, SWZ_128B);
       const uint64_t dV = smem_desc(sbase, kSlabBytes, 1024, SWZ_128B);
@@ -461,48 +506,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV3 = smem_desc(sbase + 6 * kSlabBytes, C::kOnesOff - 6 * kSlabBytes, 1024,
                                      SWZ_128B);
       const uint64_t dP = smem_desc(sbase + C::kPOff, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
+      const uint32_t hi = static_cast<uint32_t>(dK >> 32);   // same for dQ, dV, dV3
+      const uint32_t hiP = static_cast<uint32_t>(dP >> 32);
+      uint32_t lK = static_cast<uint32_t>(dK), lQ = static_cast<uint32_t>(dQ);
+      uint32_t lV = static_cast<uint32_t>(dV), lV3 = static_cast<uint32_t>(dV3);
+      uint32_t lP = static_cast<uint32_t>(dP);
+      // Makes the bases opaque, so each MMA's operands are one add at the point of
+      // use rather than values computed ahead (the issuer runs on few registers).
+      auto opaque = [&]() { asm volatile("" : "+r"(lK), "+r"(lQ), "+r"(lV), "+r"(lV3), "+r"(lP)); };
       auto qk_slab = [&](int j, uint32_t idesc, bool first) {
-#pragma unroll 1
+#pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ss(tS, dK + static_cast<uint64_t>((j * kSlabBytes + k * 32) >> 4),
-                     dQ + static_cast<uint64_t>((j * C::kQChunk + k * 32) >> 4), idesc,
-                     (first && k == 0) ? 0u : 1u);
+          mma_f16_ss_hl(tS, lK + static_cast<uint32_t>((j * kSlabBytes + k * 32) >> 4), hi,
+                        lQ + static_cast<uint32_t>((j * C::kQChunk + k * 32) >> 4), hi, idesc,
+                        (first && k == 0) ? 0u : 1u);
+      };
+      auto wait = [&](int i, uint32_t par) {
+        const bool r = wait_or_abort(bar(i), par, abort_f);
+        tc_fence_after();
+        opaque();
+        return r;
       };
       bool ok = true;
-      for (int it = 0; it < sp.ntiles && ok; ++it) {
+      for (int it = 0; it < sp.ntiles; ++it) {
         const uint32_t par = it & 1;
         // scores: rope slab first (written earliest), then the nope parts in order
-        ok = wait_or_abort(bar(B_FR), par, abort_f);
-        if (!ok) break;
-        tc_fence_after();
+        if (!(ok = wait(B_FR, par))) break;
         qk_slab(7, kIdescQKRope, true);
-#pragma unroll 1
-        for (int p = 0; p < 4; ++p) {
-          ok = wait_or_abort(bar(B_F0 + p), par, abort_f);
-          if (!ok) break;
-          tc_fence_after();
-          qk_slab(2 * p, kIdescQK, false);
-          if (p < 3) qk_slab(2 * p + 1, kIdescQK, false);
-        }
-        if (!ok) break;
+        if (!(ok = wait(B_F0, par))) break;
+        qk_slab(0, kIdescQK, false);
+        qk_slab(1, kIdescQK, false);
+        if (!(ok = wait(B_F1, par))) break;
+        qk_slab(2, kIdescQK, false);
+        qk_slab(3, kIdescQK, false);
+        if (!(ok = wait(B_F2, par))) break;
+        qk_slab(4, kIdescQK, false);
+        qk_slab(5, kIdescQK, false);
+        if (!(ok = wait(B_F3, par))) break;
+        qk_slab(6, kIdescQK, false);
         mma_commit(bar(B_SFULL));
-        ok = wait_or_abort(bar(B_PFULL), par, abort_f);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
+        if (!(ok = wait(B_PFULL, par))) break;
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+#pragma unroll
         for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll 1
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = mb < 3
-                ? dV + static_cast<uint64_t>((2 * mb * kSlabBytes + ks * 2048) >> 4)
-                : dV3 + static_cast<uint64_t>(ks * 128) - (static_cast<uint64_t>(ks * 128) << 16);
-            mma_f16_ss(tO + mb * NH, a, dP + static_cast<uint64_t>((ks * 16 * C::kPRow) >> 4),
-                        kIdescPV, (it > 0 || ks > 0) ? 1u : 0u);
+            const uint32_t a = mb < 3
+                ? lV + static_cast<uint32_t>((2 * mb * kSlabBytes + ks * 2048) >> 4)
+                : lV3 + static_cast<uint32_t>(ks * 128) - (static_cast<uint32_t>(ks * 128) << 16);
+            mma_f16_ss_hl(tO + mb * NH, a, hi,
+                          lP + static_cast<uint32_t>((ks * 16 * C::kPRow) >> 4), hiP, kIdescPV,
+                          ks > 0 ? 1u : acc0);
           }
           mma_commit(bar(B_E0 + mb));
+          opaque();
         }
       }
       mma_commit(bar(B_ODONE));
+      // Let the tensor pipe drain before the final barrier (tensor memory is freed
+      // after it), also when the workers left early.
+      if (!ok) mbar_wait(bar(B_ODONE), 0, kWaitLimit);
     }
     __syncwarp();
   } else {
@@ -539,24 +602,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint4 c[2][kSlots];
     bool s_cur[2] = {false, false};
-    int nidx[2] = {-1, -1};                      // row ids of the next tile
-    bool ok = true;
+    int nraw[2] = {-1, -1};                      // stored indices of the next tile's rows
+    int vraw = -1;                               // stored index of this thread's score row
+    const bool poller = wt == 0;
+    bool ok = sp.ntiles > 0;
     int cur = 0;                                 // which half of mbuf holds the running max
-    bool valid_next = false;
 
-    if (sp.ntiles > 0) {
-      // ---- prologue: indices, Q, the first tile's rows ----
+    if (ok) {
+      // ---- prologue: indices, the first tile's rows, Q ----
       int i0[2];
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        i0[g] = slot_row(idx_row, sp.t_begin + rr[g], sp.t_end, num_rows, lane_q0);
-        if (sp.ntiles > 1)
-          nidx[g] = slot_row(idx_row, sp.t_begin + kTile + rr[g], sp.t_end, num_rows, lane_q0);
+        i0[g] = raw_idx(idx_row, sp.t_begin + rr[g], sp.t_end);
+        nraw[g] = sp.ntiles > 1 ? raw_idx(idx_row, sp.t_begin + kTile + rr[g], sp.t_end) : -1;
       }
-      valid_next = slot_row(idx_row, sp.t_begin + r_s, sp.t_end, num_rows, false) >= 0;
+      vraw = raw_idx(idx_row, sp.t_begin + r_s, sp.t_end);
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        const uint8_t* row = i0[g] >= 0 ? kv + static_cast<int64_t>(i0[g]) * stride : nullptr;
+        const uint8_t* row = idx_ok(i0[g], num_rows, lane_q0)
+                                 ? kv + static_cast<int64_t>(i0[g]) * stride : nullptr;
         const uint8_t* base = reinterpret_cast<const uint8_t*>(
             reinterpret_cast<uintptr_t>(row) & ~static_cast<uintptr_t>(15));
         const bool sh = ((reinterpret_cast<uintptr_t>(row) >> 3) & 1) != 0;
@@ -567,57 +631,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         c[g][3] = load_slot<3>(base, q8, sh);
         c[g][4] = load_slot<4>(base, q8, sh);
       }
-      // Q rows h0..h0+NH-1 -> 8 K-major SW128 slabs (nope as f16, rope as bf16), in
-      // batches of up to 4 loads per thread
-      constexpr int kQPer = NH * 64 / kWorkers;
-      constexpr int kQBatch = kQPer < 4 ? kQPer : 4;
-      bool q_bad = false;
+      // Q rows h0..h0+NH-1 (bf16, copied into the tile area) -> 8 K-major SW128 slabs,
+      // nope as f16, rope as bf16
+      ok = workers_wait(bar(B_QRAW), 0, abort_f, poller);
+      if (ok) {
+        constexpr int kQPer = NH * 64 / kWorkers;
+        bool q_bad = false;
 #pragma unroll
-      for (int k0 = 0; k0 < kQPer; k0 += kQBatch) {
-      uint4 qv[kQBatch];
-#pragma unroll
-      for (int k = 0; k < kQBatch; ++k) {
-        const int u = wt + (k0 + k) * kWorkers, r = u >> 6, cu = u & 63;
-        qv[k] = __ldg(reinterpret_cast<const uint4*>(
-            q + (static_cast<int64_t>(b) * H + h0 + r) * kQkDim + cu * 8));
-      }
-#pragma unroll
-      for (int k = 0; k < kQBatch; ++k) {
-        const int u = wt + (k0 + k) * kWorkers, r = u >> 6, cu = u & 63;
-        uint4 o = qv[k];
-        if (cu < 56) {
-          const uint2 lo = bf16x4_to_f16x4(make_uint2(o.x, o.y));
-          const uint2 hi = bf16x4_to_f16x4(make_uint2(o.z, o.w));
-          q_bad |= f16x2_has_inf_or_nan(lo.x) | f16x2_has_inf_or_nan(lo.y) |
-                   f16x2_has_inf_or_nan(hi.x) | f16x2_has_inf_or_nan(hi.y);
-          o = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        for (int k = 0; k < kQPer; ++k) {
+          const int u = wt + k * kWorkers, r = u >> 6, cu = u & 63;
+          uint4 o = ld_shared_v4(sbase + r * 1024 + cu * 16);
+          if (cu < 56) {
+            const uint2 lo = bf16x4_to_f16x4(make_uint2(o.x, o.y));
+            const uint2 hi = bf16x4_to_f16x4(make_uint2(o.z, o.w));
+            q_bad |= f16x2_has_inf_or_nan(lo.x) | f16x2_has_inf_or_nan(lo.y) |
+                     f16x2_has_inf_or_nan(hi.x) | f16x2_has_inf_or_nan(hi.y);
+            o = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+          st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), o);
         }
-        st_shared_v4(sbase + C::kQOff + (cu >> 3) * C::kQChunk + swz_offset(r, cu & 7, 128), o);
+        if (q_bad) record_status(SMLA_ERR_RANGE);
+        if (wt < 128) {   // the constant block: 16 rows x 8 units of 16 B
+          const uint32_t r = wt >> 3, unit = wt & 7;
+          const uint4 v = make_uint4(unit == 0 ? 0x3C00u : 0u, 0u, 0u, 0u);   // f16 1.0
+          st_shared_v4(sbase + C::kOnesOff + (r >> 3) * 1024 + swz_offset(r & 7, unit, 128), v);
+        }
       }
-      }
-      if (q_bad) record_status(SMLA_ERR_RANGE);
-      if (wt < 128) {   // the constant block: 16 rows x 8 units of 16 B
-        const uint32_t r = wt >> 3, unit = wt & 7;
-        const uint4 v = make_uint4(unit == 0 ? 0x3C00u : 0u, 0u, 0u, 0u);   // f16 1.0
-        st_shared_v4(sbase + C::kOnesOff + (r >> 3) * 1024 + swz_offset(r & 7, unit, 128), v);
-      }
+      workers_bar();   // the staged q is consumed before the tile area is written
     }
 
-    for (int it = 0; it < sp.ntiles; ++it) {
+    for (int it = 0; ok && it < sp.ntiles; ++it) {
       const bool has_next = it + 1 < sp.ntiles;
       // ---- rows of the next tile (fetched while this one is converted) ----
       const uint8_t* nbase[2];
       bool ns[2];
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        const uint8_t* row =
-            (has_next && nidx[g] >= 0) ? kv + static_cast<int64_t>(nidx[g]) * stride : nullptr;
+        const uint8_t* row = (has_next && idx_ok(nraw[g], num_rows, lane_q0))
+                                 ? kv + static_cast<int64_t>(nraw[g]) * stride : nullptr;
         nbase[g] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(row) &
                                                     ~static_cast<uintptr_t>(15));
         ns[g] = ((reinterpret_cast<uintptr_t>(row) >> 3) & 1) != 0;
-        nidx[g] = it + 2 < sp.ntiles
-                      ? slot_row(idx_row, sp.t_begin + (it + 2) * kTile + rr[g], sp.t_end,
-                                 num_rows, lane_q0)
+        nraw[g] = it + 2 < sp.ntiles
+                      ? raw_idx(idx_row, sp.t_begin + (it + 2) * kTile + rr[g], sp.t_end)
                       : -1;
       }
       // ---- per-row scale words of this tile ----
@@ -722,32 +778,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(fb));
       };
-      auto wait_free = [&](int eb) {
-        if (it > 0 && ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(eb), (it - 1) & 1, abort_f));
+      // the value block that last read slabs of this part is done (no wait on tile 0)
+      auto free_wait = [&](int eb) {
+        return it == 0 || workers_wait(bar(eb), (it - 1) & 1, abort_f, poller);
       };
-      wait_free(B_E0);
-      if (ok) convert_pair(std::integral_constant<int, 0>{});
+      if (!(ok = free_wait(B_E0))) break;
+      convert_pair(std::integral_constant<int, 0>{});
       release(B_F0);
       if (has_next) {
         c[0][0] = load_slot<0>(nbase[0], q8, ns[0]);
         c[1][0] = load_slot<0>(nbase[1], q8, ns[1]);
       }
-      wait_free(B_E1);
-      if (ok) convert_pair(std::integral_constant<int, 1>{});
+      if (!(ok = free_wait(B_E1))) break;
+      convert_pair(std::integral_constant<int, 1>{});
       release(B_F1);
       if (has_next) {
         c[0][1] = load_slot<1>(nbase[0], q8, ns[0]);
         c[1][1] = load_slot<1>(nbase[1], q8, ns[1]);
       }
-      wait_free(B_E2);
-      if (ok) convert_pair(std::integral_constant<int, 2>{});
+      if (!(ok = free_wait(B_E2))) break;
+      convert_pair(std::integral_constant<int, 2>{});
       release(B_F2);
       if (has_next) {
         c[0][2] = load_slot<2>(nbase[0], q8, ns[0]);
         c[1][2] = load_slot<2>(nbase[1], q8, ns[1]);
       }
-      wait_free(B_E3);
-      if (ok) convert_slab6();
+      if (!(ok = free_wait(B_E3))) break;
+      convert_slab6();
       release(B_F3);
       if (has_next) {
         c[0][3] = load_slot<3>(nbase[0], q8, ns[0]);
@@ -757,17 +814,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_cur[1] = ns[1];
 
       // ---- softmax of this tile ----
-      const bool valid = valid_next;
-      if (has_next)
-        valid_next = slot_row(idx_row, sp.t_begin + (it + 1) * kTile + r_s, sp.t_end, num_rows,
-                              false) >= 0;
-      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(B_SFULL), it & 1, abort_f));
+      const bool valid = idx_ok(vraw, num_rows, false);
+      vraw = has_next ? raw_idx(idx_row, sp.t_begin + (it + 1) * kTile + r_s, sp.t_end) : -1;
+      if (!(ok = workers_wait(bar(B_SFULL), it & 1, abort_f, poller))) break;
+      tc_fence_after();
       float sv[HW];
       float ex = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        tmem_ld<HW>(tS + lane_base + hq * HW, sv);
-        tmem_wait_ld();
+      tmem_ld<HW>(tS + lane_base + hq * HW, sv);
+      tmem_wait_ld();
+      {
         const float* m_old = mbuf + cur * NH + hq * HW;
 #pragma unroll
         for (int i = 0; i < HW; ++i) {
@@ -776,13 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!valid) ex = -INFINITY;
       }
-      // One barrier in the common case: nobody aborted and no score passed the
-      // running max by more than the headroom.
-      if (workers_bar_or(!ok || ex > kLazyMax)) {
-        if (workers_bar_or(!ok)) {   // leave together
-          ok = false;
-          break;
-        }
+      // One barrier in the common case: no score passed the running max by more
+      // than the headroom.
+      if (workers_bar_or(ex > kLazyMax)) {
         // Raise the running max to the exact tile max and rescale O (and with it
         // the denominator row) by 2^(m_old - m_new).
 #pragma unroll
@@ -855,8 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================== epilogue =====================
-    const bool have_o = !workers_bar_or(
-        !(sp.ntiles > 0 && ok && wait_or_abort(bar(B_ODONE), 0, abort_f)));
+    // ok is the same in every worker here (all its changes came from uniform waits)
+    const bool have_o = ok && workers_wait(bar(B_ODONE), 0, abort_f, poller);
     if (have_o) tc_fence_after();
     if (qd == 2) {
       // row 448 of block 3 (TMEM lane 64: lane 0 of quarter 2) = sum_t P[t] per head
