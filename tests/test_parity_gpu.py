@@ -152,7 +152,7 @@ def test_index_out_of_range_is_skipped_and_reported():
 # ---------------------------------------------------------------------------
 # combine kernel against the oracle merge
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("S", [1, 3, 33, 200])
+@pytest.mark.parametrize("S", [1, 2, 3, 6, 9, 33, 200])
 def test_combine_matches_oracle(S):
     g = torch.Generator(device="cuda").manual_seed(S)
     B, H = 3, 16
