@@ -5,9 +5,9 @@ One step = one whole decode call (split kernel + combine kernel) for the
 batch-32 / 64-head / top-2048 workload (65536 cached rows per sequence, half the
 picks from the last 4096 positions), inputs resident in HBM.  Between steps the
 L2 is flushed (a 256 MiB write) and the index set rotates over 8 independent draws,
-so every step reads its rows from HBM.  Each step is timed with CUDA events on the
-launching stream; the split kernel is also timed on its own (events around it) for
-the roofline line.
+so every step reads its rows from HBM.  Each step is one CUDA-graph replay (a graph
+per index set) timed with CUDA events on the launching stream; the split kernel is
+also timed on its own (graphs holding only it) for the roofline line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -209,7 +209,8 @@ def config_dict(w, S):
             "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
             "row_bytes": W.ROW_BYTES, "num_splits": S,
             "index_sets": N_INDEX_SETS,
-            "l2": "flushed between steps (256 MiB write) + 8 rotating index sets"}
+            "l2": "flushed between steps (256 MiB write) + 8 rotating index sets",
+            "timing": "CUDA-graph replays (one graph per index set), events around each replay"}
 
 
 def run_gpu(args):
@@ -250,8 +251,28 @@ def run_gpu(args):
     if smla.smla_device_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
+    # One CUDA graph per index set: the whole step (split + combine), and the split
+    # kernel alone for the roofline line.  Replays are timed with events on the
+    # launching stream; the L2 flush runs outside the graphs, before each replay.
+    g_step, g_split = [], []
+    for i in range(N_INDEX_SETS):
+        for lst, with_combine in ((g_step, True), (g_split, False)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                smla.sparse_mla_decode_split(q, kv, idx_sets[i], S, w.softmax_scale,
+                                             o_part=o_part, lse_part=lse_part)
+                if with_combine:
+                    smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse)
+            lst.append(g)
+    for i in range(3):
+        flush.zero_()
+        g_step[i % N_INDEX_SETS].replay()
+        g_split[i % N_INDEX_SETS].replay()
+    torch.cuda.synchronize(dev)
+
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
@@ -260,19 +281,22 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     for i in range(K):
         flush.zero_()
-        e0, e1, e2 = ev[i]
-        e0.record(stream)
-        smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
-                                     o_part=o_part, lse_part=lse_part, stream=stream)
-        e1.record(stream)
-        smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse, stream=stream)
-        e2.record(stream)
+        ev[i][0].record(stream)
+        g_step[i % N_INDEX_SETS].replay()
+        ev[i][1].record(stream)
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        g_split[i % N_INDEX_SETS].replay()
+        evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
-    split_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    if smla.smla_device_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    split_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(step_ms)
     split_mean = statistics.mean(split_ms)
 
@@ -331,7 +355,7 @@ def run_gpu(args):
                      "tensor_tflops": tc_achieved},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
