@@ -1,13 +1,15 @@
 #!/usr/bin/env python3
 """Benchmark of the sparse MLA decode hot path on GB300.
 
-One step = one whole decode call (split kernel + combine kernel) for the
-batch-32 / 64-head / top-2048 workload (65536 cached rows per sequence, half the
-picks from the last 4096 positions), inputs resident in HBM.  Between steps the
-L2 is flushed (a 256 MiB write) and the index set rotates over 8 independent draws,
-so every step reads its rows from HBM.  Each step is one CUDA-graph replay (a graph
-per index set) timed with CUDA events on the launching stream; the split kernel is
-also timed on its own (graphs holding only it) for the roofline line.
+One step = one whole decode call, sparse_mla_decode (the split kernel with the splits
+of each query merged on chip; split + combine kernels when the plan has more than 8
+splits), for the batch-32 / 64-head / top-2048 workload (65536 cached rows per
+sequence, half the picks from the last 4096 positions), inputs resident in HBM.
+Between steps the L2 is flushed (a 256 MiB write) and the index set rotates over 8
+independent draws, so every step reads its rows from HBM.  Each step is one
+CUDA-graph replay (a graph per index set) timed with CUDA events on the launching
+stream; with two kernels per step the split kernel is also timed on its own (graphs
+holding only it) for the roofline line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -204,10 +206,10 @@ def job_throughput(world_size, batch, ms_per_step):
     return world_size * batch / (ms_per_step * 1e-3)
 
 
-def config_dict(w, S):
+def config_dict(w, S, fused=None):
     return {"workload": w.name, "batch": w.batch, "heads": w.heads, "topk": w.topk,
             "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
-            "row_bytes": W.ROW_BYTES, "num_splits": S,
+            "row_bytes": W.ROW_BYTES, "num_splits": S, "splits_merged_on_chip": fused,
             "index_sets": N_INDEX_SETS,
             "l2": "flushed between steps (256 MiB write) + 8 rotating index sets",
             "timing": "CUDA-graph replays (one graph per index set), events around each replay"}
@@ -231,7 +233,9 @@ def run_gpu(args):
     idx_sets = [torch.as_tensor(i, device=dev) for i in idx_np]
     B, H = w.batch, w.heads
     params = smla.make_params(B, H, w.topk, kv.shape[0], kv.stride(0), w.softmax_scale)
-    S = smla.smla_default_num_splits(params)
+    S, fused = smla.smla_decode_plan(params, 0)
+    ws_bytes = smla.smla_workspace_size(params, S)
+    wspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     o_part = torch.empty((B, H, S, 448), dtype=torch.float32, device=dev)
     lse_part = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     out = torch.empty((B, H, 448), dtype=torch.bfloat16, device=dev)
@@ -240,9 +244,11 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
-        smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
-                                     o_part=o_part, lse_part=lse_part, stream=stream)
-        smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse, stream=stream)
+        smla.sparse_mla_decode(q, kv, idx_sets[i % N_INDEX_SETS], w.softmax_scale, out=out,
+                               lse=lse, num_splits=S, workspace=wspace, stream=stream)
+        if not fused:
+            smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
+                                         o_part=o_part, lse_part=lse_part, stream=stream)
 
     for i in range(args.warmup):
         flush.zero_()
@@ -251,23 +257,29 @@ def run_gpu(args):
     if smla.smla_device_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # One CUDA graph per index set: the whole step (split + combine), and the split
-    # kernel alone for the roofline line.  Replays are timed with events on the
-    # launching stream; the L2 flush runs outside the graphs, before each replay.
+    # One CUDA graph per index set holding the whole step (sparse_mla_decode: one
+    # clustered launch when the plan merges the splits on chip, else split + combine)
+    # and, when the step has two kernels, graphs of the split kernel alone for the
+    # roofline line.  Replays are timed with events on the launching stream; the L2
+    # flush runs outside the graphs, before each replay.
     g_step, g_split = [], []
     for i in range(N_INDEX_SETS):
-        for lst, with_combine in ((g_step, True), (g_split, False)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            smla.sparse_mla_decode(q, kv, idx_sets[i], w.softmax_scale, out=out, lse=lse,
+                                   num_splits=S, workspace=wspace)
+        g_step.append(g)
+        if not fused:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 smla.sparse_mla_decode_split(q, kv, idx_sets[i], S, w.softmax_scale,
                                              o_part=o_part, lse_part=lse_part)
-                if with_combine:
-                    smla.sparse_mla_combine(o_part, lse_part, out=out, lse=lse)
-            lst.append(g)
+            g_split.append(g)
     for i in range(3):
         flush.zero_()
         g_step[i % N_INDEX_SETS].replay()
-        g_split[i % N_INDEX_SETS].replay()
+        if g_split:
+            g_split[i % N_INDEX_SETS].replay()
     torch.cuda.synchronize(dev)
 
     K = args.steps
@@ -284,7 +296,7 @@ def run_gpu(args):
         ev[i][0].record(stream)
         g_step[i % N_INDEX_SETS].replay()
         ev[i][1].record(stream)
-    for i in range(K):
+    for i in range(K if g_split else 0):
         flush.zero_()
         evs[i][0].record(stream)
         g_split[i % N_INDEX_SETS].replay()
@@ -296,7 +308,8 @@ def run_gpu(args):
     if smla.smla_device_status() != 0:
         raise RuntimeError("device status set during the timed region")
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    split_ms = [a.elapsed_time(b) for a, b in evs]
+    # the dominant kernel: the fused step itself, or the split kernel of a two-kernel step
+    split_ms = [a.elapsed_time(b) for a, b in evs] if g_split else step_ms
     ms = statistics.mean(step_ms)
     split_mean = statistics.mean(split_ms)
 
@@ -307,8 +320,6 @@ def run_gpu(args):
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     q_d = torch.empty_like(q)
     idx_d = torch.empty_like(idx_sets[0])
-    ws_bytes = smla.smla_workspace_size(params, S)
-    wspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     Ke = max(10, K // 4)
     ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
     for i in range(3 + Ke):
@@ -336,6 +347,8 @@ def run_gpu(args):
     hbm_peak, tc_peak, peak_kind = read_peaks()
     mean_valid_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
     split_bytes = mean_valid_bytes + q.numel() * 2 + B * w.topk * 4
+    if fused:   # the fused kernel also writes the final out and lse
+        split_bytes += out.numel() * out.element_size() + lse.numel() * 4
     achieved = split_bytes / (split_mean * 1e-3) / 1e9
     flops = statistics.mean(W.algorithmic_flops(w, i) for i in idx_np)
     tc_achieved = flops / (split_mean * 1e-3) / 1e12
@@ -344,9 +357,11 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w, S),
+        "config": config_dict(w, S, fused),
         "gathered_kv_gbs": ws * mean_valid_bytes / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm",
+                     "kernel": "split_kernel (splits merged on chip)" if fused else "split_kernel",
+                     "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_source": f"hbm_gbs ({peak_kind})", "traffic": None,
                      "algorithmic_bytes_per_launch": split_bytes,
@@ -355,7 +370,7 @@ def run_gpu(args):
                      "tensor_tflops": tc_achieved},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * K,
+        "gpu_launches": K * (1 if fused else 3),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -22,6 +22,7 @@ SMLA_ERR_SCRATCH_TOO_SMALL = -9
 
 EXPORTED = (
     "smla_default_num_splits",
+    "smla_decode_plan",
     "smla_workspace_size",
     "sparse_mla_decode",
     "sparse_mla_decode_split",
@@ -58,6 +59,7 @@ def load() -> ctypes.CDLL:
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     P = ctypes.POINTER(SmlaParams)
     lib.smla_default_num_splits.argtypes = [P, ctypes.POINTER(i32)]
+    lib.smla_decode_plan.argtypes = [P, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.smla_workspace_size.argtypes = [P, i32, ctypes.POINTER(sz)]
     lib.sparse_mla_decode.argtypes = [vp, vp, vp, vp, vp, P, i32, vp, sz, vp]
     lib.sparse_mla_decode_split.argtypes = [vp, vp, vp, P, i32, vp, vp, vp]

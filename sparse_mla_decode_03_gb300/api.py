@@ -72,6 +72,15 @@ def smla_default_num_splits(params: _lib.SmlaParams) -> int:
     return n.value
 
 
+def smla_decode_plan(params: _lib.SmlaParams, num_splits: int = 0) -> Tuple[int, bool]:
+    """(resolved split count, True if sparse_mla_decode merges the splits on chip)."""
+    lib = _lib.load()
+    S, fused = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.smla_decode_plan(ctypes.byref(params), num_splits, ctypes.byref(S),
+                                ctypes.byref(fused)), "smla_decode_plan")
+    return S.value, bool(fused.value)
+
+
 def smla_workspace_size(params: _lib.SmlaParams, num_splits: int = 0) -> int:
     lib = _lib.load()
     n = ctypes.c_size_t(0)

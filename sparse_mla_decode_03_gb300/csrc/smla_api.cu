@@ -120,6 +120,20 @@ int smla_default_num_splits(const smla_params* p, int32_t* num_splits) {
   return SMLA_OK;
 }
 
+int smla_decode_plan(const smla_params* p, int32_t num_splits, int32_t* splits, int32_t* fused) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  if (splits == nullptr || fused == nullptr) return SMLA_ERR_INVALID_ARG;
+  int S = 0;
+  st = resolve_splits(p, num_splits, &S);
+  if (st != SMLA_OK) return st;
+  bool ok = false;
+  if (smla::fused_supported(p->num_heads, S, &ok) != cudaSuccess) return SMLA_ERR_CUDA;
+  *splits = S;
+  *fused = ok ? 1 : 0;
+  return SMLA_OK;
+}
+
 int smla_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes) {
   int st = check_params(p);
   if (st != SMLA_OK) return st;
@@ -191,7 +205,14 @@ int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indice
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
+  // One launch when the splits of a query fit in a thread-block cluster (they merge
+  // their partials in the workspace inside that launch); split + combine otherwise.
+  cudaError_t e = smla::launch_decode_fused(q, kv_cache, indices, o_part, lse_part, out, lse,
+                                            p->batch, p->num_heads, p->topk, S, p->num_rows,
+                                            p->kv_row_stride, p->softmax_scale, s);
+  if (e == cudaSuccess) return SMLA_OK;
+  if (e != cudaErrorNotSupported) return SMLA_ERR_CUDA;
+  e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
                                      p->num_heads, p->topk, S, p->num_rows, p->kv_row_stride,
                                      p->softmax_scale, s);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;

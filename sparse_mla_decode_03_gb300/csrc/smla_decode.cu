@@ -16,7 +16,9 @@
 // and finally writes the normalised partial O and its log-sum-exp for the split
 // (the split-K scheme of "The 80KB Mystery: Resolving Contradictory Evidence in
 // Triton Kernel Optimization", section "The Context: Optimizing Attention on
-// Blackwell").
+// Blackwell").  Launched as thread-block clusters of the S splits of a (query, head
+// group), the CTAs then also merge the splits (the combine step) after a cluster
+// barrier, each for a slice of the heads, and write the final out and lse.
 //
 // Design (sm_103a).  Tokens are the MMA's M dimension, so every MMA is a full
 // 128-row tcgen05 instruction even with 16 heads.  The nope operands are f16 (fp32
@@ -72,6 +74,8 @@ constexpr int kLaunchRegs = 96;
 constexpr long long kWaitLimit = 2000000000LL;  // ~1 s of SM clocks
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLazyMax = 8.0f;                // log2 headroom before the max is raised
+constexpr int kMaxCluster = 8;                  // splits merged on chip (portable cluster size)
+enum : int { kSplitOnly = 0, kMergeL2 = 1 };
 
 // mbarriers.  FR: rope slab written; F0..F3: slab pairs (0,1), (2,3), (4,5) and slab
 // 6 written; E0..E3: value block 0..3 done (its slabs may be overwritten); SFULL:
@@ -170,6 +174,12 @@ __device__ __forceinline__ bool workers_bar_and(bool p) {
       : "r"(p ? 1u : 0u)
       : "memory");
   return r != 0;
+}
+
+// Barrier over every thread of every CTA of the thread-block cluster, ordering their
+// memory accesses (release before, acquire after).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // 2^x on the SFU (ex2.approx, relative error ~2^-22; subnormal results flush to 0).
@@ -431,11 +441,17 @@ struct RowPrep {
   uint32_t base_o;          // shared address of the odd word of pair 0
 };
 
-template <int NH>
+// MODE kSplitOnly: writes the split's normalised partial O and lse (o_part, lse_part).
+// MODE kMergeL2: launched as clusters of the S splits of one (query, head group); each
+//   split writes its partials as above, then after a cluster barrier each CTA merges
+//   a slice of the heads from the (L2-resident) partials of all the splits and writes
+//   the final bf16 out and lse: the split-K combine without a second launch.
+template <int NH, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ kv,
                  const int32_t* __restrict__ indices, float* __restrict__ o_part,
-                 float* __restrict__ lse_part, int H, int topk, int S, int64_t num_rows,
+                 float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out,
+                 float* __restrict__ lse_out, int H, int topk, int S, int64_t num_rows,
                  int64_t stride, float scale_log2) {
   using C = Cfg<NH>;
   constexpr int HW = C::kHW;
@@ -568,6 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) mbar_wait(bar(B_ODONE), 0, kWaitLimit);
     }
     __syncwarp();
+    // the cluster barrier of the merging epilogue, in step with the workers
+    if constexpr (MODE == kMergeL2) cluster_sync();
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsWorker) : "memory");
     // ===================== workers =====================
@@ -922,6 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     workers_bar();
+    {
     if (wt < NH) {
       const float lt = lfin[wt];
       const float lse = lt > 0.f ? (mbuf[cur * NH + wt] + log2f(lt)) * kLn2 : -INFINITY;
@@ -951,6 +970,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if constexpr (MODE == kMergeL2) {
+      cluster_sync();   // every split of this (query, head group) has written its partials
+      // this CTA merges heads [h_lo, h_hi): weights exp(lse_s - lse) per head first
+      const int h_lo = s * NH / S, h_hi = (s + 1) * NH / S, nh = h_hi - h_lo;
+      float* wgt = reinterpret_cast<float*>(smem);   // [nh][kMaxCluster] (tile area is free)
+      float* fin = wgt + NH * kMaxCluster;            // [nh] final lse (natural log)
+      if (wt < nh) {
+        const float* lp = lse_part + (static_cast<int64_t>(b) * H + h0 + h_lo + wt) * S;
+        float x[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) x[r] = r < S ? lp[r] : -INFINITY;
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, x[r]);
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          const float e = (M == -INFINITY || x[r] == -INFINITY) ? 0.f : __expf(x[r] - M);
+          x[r] = e;
+          sum += e;
+        }
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) wgt[wt * kMaxCluster + r] = x[r] * inv;
+        fin[wt] = sum > 0.f ? M + logf(sum) : -INFINITY;
+      }
+      workers_bar();
+      const int units = nh * (kNope / 4);
+      for (int u = wt; u < units; u += kWorkers) {
+        const int hl = u / (kNope / 4), d4 = u % (kNope / 4);
+        const float4* src = reinterpret_cast<const float4*>(
+            o_part + ((static_cast<int64_t>(b) * H + h0 + h_lo + hl) * S) * kNope) + d4;
+        float4 v[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < S) v[r] = __ldcg(src + r * (kNope / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < S) {
+            const float ws = wgt[hl * kMaxCluster + r];
+            acc.x = fmaf(ws, v[r].x, acc.x);
+            acc.y = fmaf(ws, v[r].y, acc.y);
+            acc.z = fmaf(ws, v[r].z, acc.z);
+            acc.w = fmaf(ws, v[r].w, acc.w);
+          }
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * H + h0 + h_lo + hl) * kNope +
+                                  4 * d4) = pk;
+      }
+      if (wt < nh) lse_out[static_cast<int64_t>(b) * H + h0 + h_lo + wt] = fin[wt];
+    }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -960,33 +1037,111 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Once per device and kernel: shared-memory size and the register check (the
+// setmaxnreg split assumes the launch allocation; a build that differs is refused,
+// since its register increase would never be granted).
+template <int NH, int MODE>
+cudaError_t configure(int dev) {
+  static int configured_device = -1;
+  if (configured_device == dev) return cudaSuccess;
+  using C = Cfg<NH>;
+  cudaError_t e = cudaFuncSetAttribute(split_kernel<NH, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, split_kernel<NH, MODE>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+  configured_device = dev;
+  return cudaSuccess;
+}
+
 template <int NH>
 cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices, float* o_part,
                            float* lse_part, int B, int H, int topk, int S, int64_t num_rows,
                            int64_t stride, float softmax_scale, cudaStream_t stream) {
   using C = Cfg<NH>;
-  static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, split_kernel<NH>);
-    if (e != cudaSuccess) return e;
-    // The setmaxnreg split assumes this launch allocation; refuse to launch a build
-    // that differs (the register increase would never be granted).
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    configured_device = dev;
-  }
+  e = configure<NH, kSplitOnly>(dev);
+  if (e != cudaSuccess) return e;
   const dim3 grid(S, H / NH, B);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
-  split_kernel<NH><<<grid, kThreads, C::kSmemBytes, stream>>>(
+  split_kernel<NH, kSplitOnly><<<grid, kThreads, C::kSmemBytes, stream>>>(
       static_cast<const uint16_t*>(q), static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
-      H, topk, S, num_rows, stride, scale_log2);
+      nullptr, nullptr, H, topk, S, num_rows, stride, scale_log2);
   return cudaGetLastError();
+}
+
+constexpr int kMaxClusterSplits = kMaxCluster;
+
+// Whether a cluster of S split CTAs fits on the device: asked once per (device, S).
+template <int NH, int MODE>
+cudaError_t cluster_fits(int dev, int S, bool* fits) {
+  static int asked_device[kMaxClusterSplits + 1] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  static bool answer[kMaxClusterSplits + 1] = {};
+  if (S < 1 || S > kMaxClusterSplits) {
+    *fits = false;
+    return cudaSuccess;
+  }
+  if (asked_device[S] != dev) {
+    cudaError_t e = configure<NH, MODE>(dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<NH>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, split_kernel<NH, MODE>, &cfg);
+    if (e != cudaSuccess) return e;
+    answer[S] = n > 0;
+    asked_device[S] = dev;
+  }
+  *fits = answer[S];
+  return cudaSuccess;
+}
+
+template <int NH, int MODE>
+cudaError_t launch_fused_t(const void* q, const void* kv, const int32_t* indices, float* o_part,
+                           float* lse_part, void* out, float* lse, int B, int H, int topk, int S,
+                           int64_t num_rows, int64_t stride, float softmax_scale,
+                           cudaStream_t stream) {
+  using C = Cfg<NH>;
+  if (S < 1 || S > kMaxClusterSplits) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = configure<NH, MODE>(dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, H / NH, B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  bool fits = false;
+  e = cluster_fits<NH, MODE>(dev, S, &fits);
+  if (e != cudaSuccess) return e;
+  if (!fits) return cudaErrorNotSupported;
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  return cudaLaunchKernelEx(&cfg, split_kernel<NH, MODE>, static_cast<const uint16_t*>(q),
+                            static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
+                            static_cast<__nv_bfloat16*>(out), lse, H, topk, S, num_rows, stride,
+                            scale_log2);
 }
 
 }  // namespace
@@ -1004,6 +1159,34 @@ cudaError_t launch_split(const void* q, const void* kv, const int32_t* indices, 
     default:  // 64 and 128 (two head groups of 64)
       return launch_split_t<64>(q, kv, indices, o_part, lse_part, B, H, topk, S, num_rows, stride,
                                 softmax_scale, stream);
+  }
+}
+
+cudaError_t launch_decode_fused(const void* q, const void* kv, const int32_t* indices,
+                                float* o_part, float* lse_part, void* out, float* lse, int B,
+                                int H, int topk, int S, int64_t num_rows, int64_t stride,
+                                float softmax_scale, cudaStream_t stream) {
+  switch (H) {
+    case 16:
+      return launch_fused_t<16, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+                                          S, num_rows, stride, softmax_scale, stream);
+    case 32:
+      return launch_fused_t<32, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+                                          S, num_rows, stride, softmax_scale, stream);
+    default:
+      return launch_fused_t<64, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+                                          S, num_rows, stride, softmax_scale, stream);
+  }
+}
+
+cudaError_t fused_supported(int H, int S, bool* supported) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  switch (H) {
+    case 16: return cluster_fits<16, kMergeL2>(dev, S, supported);
+    case 32: return cluster_fits<32, kMergeL2>(dev, S, supported);
+    default: return cluster_fits<64, kMergeL2>(dev, S, supported);
   }
 }
 

@@ -12,10 +12,23 @@ constexpr int kRowBytes = 584;  // packed KV row
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCombineSplits = 1024;
 
-// Launches the split kernel: grid (S, H / heads_per_cta, B), 128 threads.
+// Launches the split kernel: grid (S, H / heads_per_cta, B), 640 threads.
 cudaError_t launch_split(const void* q, const void* kv, const int32_t* indices, float* o_part,
                          float* lse_part, int B, int H, int topk, int S, int64_t num_rows,
                          int64_t stride, float softmax_scale, cudaStream_t stream);
+
+// Launches the split kernel as clusters of the S splits of each (query, head group):
+// the splits write o_part / lse_part, then (after a cluster barrier) each CTA merges
+// a slice of the heads from them and writes the final out / lse.  Returns
+// cudaErrorNotSupported (nothing launched) when S > 8 or such a cluster does not fit
+// on the device; the caller then uses split + combine.
+cudaError_t launch_decode_fused(const void* q, const void* kv, const int32_t* indices,
+                                float* o_part, float* lse_part, void* out, float* lse, int B,
+                                int H, int topk, int S, int64_t num_rows, int64_t stride,
+                                float softmax_scale, cudaStream_t stream);
+
+// Whether launch_decode_fused can run S splits of H heads on the current device.
+cudaError_t fused_supported(int H, int S, bool* supported);
 
 // Launches the combine kernel over B * H (batch, head) pairs.
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int H, int S,

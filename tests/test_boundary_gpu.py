@@ -75,3 +75,39 @@ def test_side_stream_and_graph_replay():
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
     assert_lse_close(lse.cpu().numpy(), rl)
+
+
+def test_plan_reports_the_on_chip_merge():
+    """The batch-32 / 64-head / top-2048 plan (4 splits) runs as one clustered launch;
+    more than 8 splits use the split + combine kernels."""
+    from sparse_mla_decode_03_gb300 import smla_decode_plan
+    p = make_params(32, 64, 2048, 32 * 65536, 584)
+    S, fused = smla_decode_plan(p, 0)
+    assert S == smla_default_num_splits(p)
+    assert fused and S <= 8
+    assert smla_decode_plan(p, 16) == (16, False)
+    assert smla_decode_plan(make_params(4, 16, 512, 4 * 16384, 584), 3) == (3, True)
+
+
+@pytest.mark.parametrize("H,S", [(64, 1), (64, 4), (32, 3), (16, 8), (128, 2)])
+def test_on_chip_merge_matches_split_and_combine(H, S):
+    """sparse_mla_decode with the merge on chip equals the split kernel followed by the
+    combine kernel on the same inputs, and both equal the oracle."""
+    from sparse_mla_decode_03_gb300 import (smla_decode_plan, sparse_mla_combine,
+                                            sparse_mla_decode_split)
+    B, k = 3, 700
+    w, kv, q, idx_np = small_case(B, H, 4000, k, seed=H + S)
+    idx_np[1, 300:] = -1
+    idx_np[2, :] = -1                        # an empty query
+    idx = torch.as_tensor(idx_np, device="cuda")
+    p = make_params(B, H, k, kv.shape[0], 584)
+    assert smla_decode_plan(p, S) == (S, True)
+    out_f, lse_f = sparse_mla_decode(q, kv, idx, num_splits=S)
+    o_part, lse_part = sparse_mla_decode_split(q, kv, idx, S)
+    out_u, lse_u = sparse_mla_combine(o_part, lse_part)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_decode(q, kv, idx_np)
+    assert_out_close(out_f.float().cpu().numpy(), ref_out)
+    assert_lse_close(lse_f.cpu().numpy(), ref_lse)
+    assert_out_close(out_f.float().cpu().numpy(), out_u.float().cpu().numpy().astype(np.float64))
+    assert np.all(out_f[2].float().cpu().numpy() == 0) and np.all(np.isneginf(lse_f[2].cpu().numpy()))
