@@ -42,6 +42,12 @@ UNIT = "queries/s"
 WORKLOAD = "c3"
 N_INDEX_SETS = 8
 FLUSH_BYTES = 256 << 20
+# DRAM bytes (read + write) per launch of the dominant kernel on this workload, from
+# one ncu capture (profiles/fused_split_kernel_c3_b32_h64_k2048.md).  They describe the
+# kernel source they were taken on: with any other source the field is null.
+TRAFFIC_KERNEL_SRC = "sparse_mla_decode_03_gb300/csrc/smla_decode.cu"
+TRAFFIC_SRC_SHA256_16 = "baeb233c508c88cb"
+TRAFFIC_BYTES = 47560192 + 479488
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -51,6 +57,17 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def measured_traffic():
+    """ncu DRAM bytes per launch, or None once the kernel source has changed."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, TRAFFIC_KERNEL_SRC), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return TRAFFIC_BYTES if sha == TRAFFIC_SRC_SHA256_16 else None
 
 
 def read_peaks():
@@ -363,7 +380,8 @@ def run_gpu(args):
                      "kernel": "split_kernel (splits merged on chip)" if fused else "split_kernel",
                      "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_source": f"hbm_gbs ({peak_kind})", "traffic": None,
+                     "peak_source": f"hbm_gbs ({peak_kind})",
+                     "traffic": measured_traffic() if fused else None,
                      "algorithmic_bytes_per_launch": split_bytes,
                      "launch_ms": split_mean,
                      "tensor_frac": tc_achieved / tc_peak,
