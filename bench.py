@@ -46,7 +46,7 @@ FLUSH_BYTES = 256 << 20
 # one ncu capture (profiles/fused_split_kernel_c3_b32_h64_k2048.md).  They describe the
 # kernel source they were taken on: with any other source the field is null.
 TRAFFIC_KERNEL_SRC = "sparse_mla_decode_03_gb300/csrc/smla_decode.cu"
-TRAFFIC_SRC_SHA256_16 = "baeb233c508c88cb"
+TRAFFIC_SRC_SHA256_16 = "6a7812e6f4191ce7"
 TRAFFIC_BYTES = 47560192 + 479488
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -330,6 +330,20 @@ def run_gpu(args):
     ms = statistics.mean(step_ms)
     split_mean = statistics.mean(split_ms)
 
+    # ---- context: the per-head fp32 SIMT form of the same step (the pages' pre-MMA
+    # kernel style), on the same inputs, outside the timed region above ----
+    simt_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(5)]
+    for i in range(6):
+        flush.zero_()
+        if i >= 1:
+            simt_ev[i - 1][0].record(stream)
+        smla.sparse_mla_decode_simt(q, kv, idx_sets[i % N_INDEX_SETS], w.softmax_scale,
+                                    out=out, lse=lse, stream=stream)
+        if i >= 1:
+            simt_ev[i - 1][1].record(stream)
+    torch.cuda.synchronize(dev)
+    simt_ms = statistics.mean(a.elapsed_time(b) for a, b in simt_ev)
+
     # ---- end to end through the C ABI, host buffers, copies inside the timed region ----
     q_h = q.cpu().pin_memory()
     idx_h = [i.cpu().pin_memory() for i in idx_sets]
@@ -389,6 +403,9 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": K * (1 if fused else 3),
+        "context": {"simt_ms_per_step": simt_ms, "tensor_core_speedup": simt_ms / ms,
+                    "simt": "sparse_mla_decode_simt: one CTA per (query, head), fp32, rows "
+                            "re-read per head; 5 plain launches, L2 flushed"},
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

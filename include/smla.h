@@ -139,6 +139,18 @@ int sparse_mla_combine(const float* o_part, const float* lse_part, int32_t batch
                        smla_stream_t stream);
 
 /*
+ * The same decode step computed the way the pages' production kernel did before the
+ * tensor-core rewrite: one CTA per (query, head), element-wise fp32 arithmetic, and
+ * every head reading the selected rows again ("The Moment of Compilation: When a
+ * Triton Kernel Meets Its Constraints", sections "The Context: A Kernel
+ * Optimization Campaign" and "The Assumption That Broke").  It is a same-device
+ * reference point for the tensor-core path, not a faster alternative.  Arguments as
+ * for sparse_mla_decode (no workspace, no splits); batch <= 65535.
+ */
+int sparse_mla_decode_simt(const void* q, const void* kv_cache, const int32_t* indices,
+                           void* out, float* lse, const smla_params* p, smla_stream_t stream);
+
+/*
  * sparse_mla_decode without a caller-provided workspace.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory: for example code that runs inside another framework's memory

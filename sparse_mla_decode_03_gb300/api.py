@@ -177,6 +177,25 @@ def sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: 
     return out, lse
 
 
+def sparse_mla_decode_simt(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                           softmax_scale: float = DEFAULT_SCALE,
+                           out: Optional[torch.Tensor] = None,
+                           lse: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None
+                           ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The per-head fp32 SIMT form of the decode step (a reference point for the
+    tensor-core path).  Returns (out bf16 [B, H, 448], lse fp32 [B, H])."""
+    p = _params_from(q, kv_cache, indices, softmax_scale)
+    if out is None:
+        out = torch.empty((p.batch, p.num_heads, NOPE), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_heads), dtype=torch.float32, device=q.device)
+    st = _lib.load().sparse_mla_decode_simt(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(out),
+                                            _ptr(lse), ctypes.byref(p), _stream(stream))
+    _check(st, "sparse_mla_decode_simt")
+    return out, lse
+
+
 def smla_device_status(clear: bool = False) -> int:
     """Device status word (0, SMLA_ERR_TIMEOUT or SMLA_ERR_INDEX_RANGE); synchronises."""
     lib = _lib.load()

@@ -220,6 +220,24 @@ int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indice
   return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
+int sparse_mla_decode_simt(const void* q, const void* kv_cache, const int32_t* indices,
+                           void* out, float* lse, const smla_params* p, smla_stream_t stream) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  st = check_tensors(q, kv_cache, indices);
+  if (st != SMLA_OK) return st;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  if (p->batch > 65535) return SMLA_ERR_UNSUPPORTED_SHAPE;
+  int sms = 0;
+  st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  const cudaError_t e = smla::launch_simt(q, kv_cache, indices, out, lse, p->batch, p->num_heads,
+                                          p->topk, p->num_rows, p->kv_row_stride,
+                                          p->softmax_scale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
 const char* smla_status_string(int status) {
   switch (status) {
     case SMLA_OK: return "SMLA_OK";

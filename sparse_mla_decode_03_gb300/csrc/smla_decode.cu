@@ -1190,6 +1190,10 @@ cudaError_t fused_supported(int H, int S, bool* supported) {
   }
 }
 
+cudaError_t status_word_address(int** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_smla_status);
+}
+
 cudaError_t read_device_status(int32_t* status, bool clear) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return e;

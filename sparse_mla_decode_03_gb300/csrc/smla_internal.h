@@ -34,6 +34,15 @@ cudaError_t fused_supported(int H, int S, bool* supported);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int H, int S,
                            void* out, float* lse, cudaStream_t stream);
 
+// Launches the per-head SIMT decode (one CTA per (query, head), fp32 arithmetic).
+cudaError_t launch_simt(const void* q, const void* kv, const int32_t* indices, void* out,
+                        float* lse, int B, int H, int topk, int64_t num_rows, int64_t stride,
+                        float softmax_scale, cudaStream_t stream);
+
+// Device address of the status word (kernels in other translation units record
+// their errors through it; device variables are not shared across them).
+cudaError_t status_word_address(int** ptr);
+
 // Device status word (first error wins).
 cudaError_t read_device_status(int32_t* status, bool clear);
 
