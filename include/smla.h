@@ -139,6 +139,29 @@ int sparse_mla_combine(const float* o_part, const float* lse_part, int32_t batch
                        smla_stream_t stream);
 
 /*
+ * The decode step over a paged cache.  "The Power-of-Two Trap: Debugging a Triton MMA
+ * Kernel on Blackwell GPUs", section "Input Knowledge Required", says the KV cache is
+ * paged but gives no layout; this entry point takes the usual one:
+ *   kv_pages    uint8 [num_rows, kv_row_stride]: a pool of pages of page_size
+ *               consecutive rows (num_rows = pool rows, params as for
+ *               sparse_mla_decode), 16-byte aligned
+ *   block_table int32 [B, max_pages_per_seq]: page ids of each query's sequence,
+ *               < 0 = unmapped page
+ *   indices     int32 [B, topk]: logical token positions in the sequence, < 0 = masked
+ * Position t of query b is row block_table[b][t / page_size] * page_size +
+ * t % page_size.  Positions on an unmapped page are masked; positions past the table
+ * or rows past the pool are masked and reported as SMLA_ERR_INDEX_RANGE in the
+ * device status word.  The workspace (smla_paged_workspace_size bytes, 256-byte
+ * aligned) also holds the translated rows; a small translation kernel runs first,
+ * then the decode as in sparse_mla_decode.  page_size >= 1, max_pages_per_seq >= 1.
+ */
+int smla_paged_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes);
+int sparse_mla_decode_paged(const void* q, const void* kv_pages, const int32_t* block_table,
+                            int32_t max_pages_per_seq, int32_t page_size, const int32_t* indices,
+                            void* out, float* lse, const smla_params* p, int32_t num_splits,
+                            void* workspace, size_t workspace_bytes, smla_stream_t stream);
+
+/*
  * The same decode step computed the way the pages' production kernel did before the
  * tensor-core rewrite: one CTA per (query, head), element-wise fp32 arithmetic, and
  * every head reading the selected rows again ("The Moment of Compilation: When a

@@ -5,7 +5,7 @@
 """
 from .api import (  # noqa: F401
     DEFAULT_SCALE, SmlaError, make_params, smla_decode_plan, smla_default_num_splits,
-    smla_device_status,
+    smla_device_status, smla_paged_workspace_size, sparse_mla_decode_paged,
     smla_status_string, smla_workspace_size, sparse_mla_combine, sparse_mla_decode,
     sparse_mla_decode_noalloc, sparse_mla_decode_simt, sparse_mla_decode_split,
 )

@@ -29,6 +29,8 @@ EXPORTED = (
     "sparse_mla_combine",
     "sparse_mla_decode_noalloc",
     "sparse_mla_decode_simt",
+    "smla_paged_workspace_size",
+    "sparse_mla_decode_paged",
     "smla_status_string",
     "smla_device_status",
 )
@@ -67,6 +69,8 @@ def load() -> ctypes.CDLL:
     lib.sparse_mla_combine.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     lib.sparse_mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, i32, vp]
     lib.sparse_mla_decode_simt.argtypes = [vp, vp, vp, vp, vp, P, vp]
+    lib.smla_paged_workspace_size.argtypes = [P, i32, ctypes.POINTER(sz)]
+    lib.sparse_mla_decode_paged.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, P, i32, vp, sz, vp]
     lib.smla_status_string.argtypes = [ctypes.c_int]
     lib.smla_status_string.restype = ctypes.c_char_p
     lib.smla_device_status.argtypes = [ctypes.POINTER(i32), i32]

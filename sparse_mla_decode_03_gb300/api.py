@@ -177,6 +177,43 @@ def sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, indices: 
     return out, lse
 
 
+def smla_paged_workspace_size(params: _lib.SmlaParams, num_splits: int = 0) -> int:
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _check(lib.smla_paged_workspace_size(ctypes.byref(params), num_splits, ctypes.byref(n)),
+           "smla_paged_workspace_size")
+    return n.value
+
+
+def sparse_mla_decode_paged(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                            page_size: int, indices: torch.Tensor,
+                            softmax_scale: float = DEFAULT_SCALE,
+                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None
+                            ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Decode step over a paged cache: `indices` are logical positions in each query's
+    sequence, `block_table` int32 [B, max_pages] maps its pages into `kv_pages`."""
+    p = _params_from(q, kv_pages, indices, softmax_scale)
+    if (block_table.dim() != 2 or block_table.dtype != torch.int32
+            or block_table.shape[0] != p.batch or not block_table.is_contiguous()
+            or not block_table.is_cuda):
+        raise ValueError("block_table must be a contiguous CUDA int32 [B, max_pages] tensor")
+    if out is None:
+        out = torch.empty((p.batch, p.num_heads, NOPE), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_heads), dtype=torch.float32, device=q.device)
+    need = smla_paged_workspace_size(p, num_splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = _lib.load().sparse_mla_decode_paged(
+        _ptr(q), _ptr(kv_pages), _ptr(block_table), block_table.shape[1], page_size,
+        _ptr(indices), _ptr(out), _ptr(lse), ctypes.byref(p), num_splits, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "sparse_mla_decode_paged")
+    return out, lse
+
+
 def sparse_mla_decode_simt(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
                            softmax_scale: float = DEFAULT_SCALE,
                            out: Optional[torch.Tensor] = None,

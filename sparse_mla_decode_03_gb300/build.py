@@ -18,7 +18,8 @@ LIB = os.path.join(HERE, "libsmla.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", os.path.join(ROOT, "include")]
-SOURCES = ["smla_decode.cu", "smla_combine.cu", "smla_api.cu", "smla_noalloc.cu", "smla_simt.cu"]
+SOURCES = ["smla_decode.cu", "smla_combine.cu", "smla_api.cu", "smla_noalloc.cu", "smla_simt.cu",
+           "smla_paged.cu"]
 
 
 def nvcc() -> str:

@@ -220,6 +220,42 @@ int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indice
   return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
+int smla_paged_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes) {
+  size_t total = 0;
+  const int st = smla_workspace_size(p, num_splits, &total);
+  if (st != SMLA_OK) return st;
+  *bytes = total + round256(static_cast<size_t>(p->batch) * p->topk * sizeof(int32_t));
+  return SMLA_OK;
+}
+
+int sparse_mla_decode_paged(const void* q, const void* kv_pages, const int32_t* block_table,
+                            int32_t max_pages_per_seq, int32_t page_size, const int32_t* indices,
+                            void* out, float* lse, const smla_params* p, int32_t num_splits,
+                            void* workspace, size_t workspace_bytes, smla_stream_t stream) {
+  int st = check_params(p);
+  if (st != SMLA_OK) return st;
+  st = check_tensors(q, kv_pages, indices);
+  if (st != SMLA_OK) return st;
+  if (block_table == nullptr || !aligned(block_table, 4) || max_pages_per_seq < 1 || page_size < 1)
+    return SMLA_ERR_INVALID_ARG;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return SMLA_ERR_INVALID_ARG;
+  size_t total = 0, need = 0;
+  st = smla_workspace_size(p, num_splits, &total);
+  if (st != SMLA_OK) return st;
+  st = smla_paged_workspace_size(p, num_splits, &need);
+  if (st != SMLA_OK) return st;
+  if (workspace_bytes < need) return SMLA_ERR_WORKSPACE_TOO_SMALL;
+  // the translated rows sit after the decode's own part of the workspace
+  int32_t* rows = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + total);
+  const cudaError_t e = smla::launch_paged_rows(indices, block_table, p->batch, p->topk,
+                                                max_pages_per_seq, page_size, p->num_rows, rows,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return SMLA_ERR_CUDA;
+  return sparse_mla_decode(q, kv_pages, rows, out, lse, p, num_splits, workspace, total, stream);
+}
+
 int sparse_mla_decode_simt(const void* q, const void* kv_cache, const int32_t* indices,
                            void* out, float* lse, const smla_params* p, smla_stream_t stream) {
   int st = check_params(p);

@@ -39,6 +39,11 @@ cudaError_t launch_simt(const void* q, const void* kv, const int32_t* indices, v
                         float* lse, int B, int H, int topk, int64_t num_rows, int64_t stride,
                         float softmax_scale, cudaStream_t stream);
 
+// Translates logical positions of a paged cache into pool rows (-1 = masked).
+cudaError_t launch_paged_rows(const int32_t* indices, const int32_t* block_table, int B, int topk,
+                              int max_pages, int page_size, int64_t num_rows, int32_t* rows,
+                              cudaStream_t stream);
+
 // Device address of the status word (kernels in other translation units record
 // their errors through it; device variables are not shared across them).
 cudaError_t status_word_address(int** ptr);

@@ -87,3 +87,28 @@ def test_null_pointers_rejected_before_any_launch(lib):
     assert st == _lib.SMLA_ERR_INVALID_ARG
     st = lib.sparse_mla_combine(vp(0), vp(0), 1, 1, 1, vp(0), vp(0), vp(0))
     assert st == _lib.SMLA_ERR_INVALID_ARG
+
+
+def test_paged_workspace_adds_the_translated_rows(lib):
+    p = make_params(32, 64, 2048, 1 << 20, 584)
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.smla_workspace_size(ctypes.byref(p), 4, ctypes.byref(a)) == 0
+    assert lib.smla_paged_workspace_size(ctypes.byref(p), 4, ctypes.byref(b)) == 0
+    assert b.value == a.value + (32 * 2048 * 4 + 255) // 256 * 256
+
+
+def test_paged_argument_checks(lib):
+    p = make_params(2, 64, 128, 1000, 584)
+    vp = ctypes.c_void_p
+    args = (vp(16), vp(16), vp(16))
+    # null block table, bad page size, bad table width: rejected before any launch
+    assert lib.sparse_mla_decode_paged(vp(16), vp(16), vp(0), 4, 16, vp(16), vp(16), vp(16),
+                                       ctypes.byref(p), 0, vp(256), 1 << 20, vp(0)) == \
+        _lib.SMLA_ERR_INVALID_ARG
+    assert lib.sparse_mla_decode_paged(vp(16), vp(16), vp(16), 4, 0, vp(16), vp(16), vp(16),
+                                       ctypes.byref(p), 0, vp(256), 1 << 20, vp(0)) == \
+        _lib.SMLA_ERR_INVALID_ARG
+    assert lib.sparse_mla_decode_paged(vp(16), vp(16), vp(16), 0, 16, vp(16), vp(16), vp(16),
+                                       ctypes.byref(p), 0, vp(256), 1 << 20, vp(0)) == \
+        _lib.SMLA_ERR_INVALID_ARG
+    del args
