@@ -5,11 +5,18 @@ One step = one whole decode call, sparse_mla_decode (the split kernel with the s
 of each query merged on chip; split + combine kernels when the plan has more than 8
 splits), for the batch-32 / 64-head / top-2048 workload (65536 cached rows per
 sequence, half the picks from the last 4096 positions), inputs resident in HBM.
-Between steps the L2 is flushed (a 256 MiB write) and the index set rotates over 8
-independent draws, so every step reads its rows from HBM.  Each step is one
-CUDA-graph replay (a graph per index set) timed with CUDA events on the launching
-stream; with two kernels per step the split kernel is also timed on its own (graphs
-holding only it) for the roofline line.
+
+Steps run back to back, as the attention of consecutive layers does: step i decodes
+layer i mod NL, and every layer has its own KV cache, q and index set.  NL is chosen
+so that at least three L2 capacities of other layers' rows are read between two
+reads of one layer, so the rows of every step come from HBM (inputs larger than L2;
+no flush).  The steps are captured in CUDA graphs of up to 128 calls, replayed with
+one pair of CUDA events around exactly K steps on the launching stream; the kernels
+use programmatic dependent launch, so a step's launch overlaps the end of the one
+before.  Workloads whose data cannot exceed L2 (the batch-1 and batch-4 shapes) are
+timed one isolated step at a time instead: L2 flushed (a 256 MiB write) before each
+step, events around each single-step graph replay.  The isolated time is reported
+for every workload as context.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -40,8 +47,11 @@ from sparse_mla_decode_03_gb300 import workloads as W  # noqa: E402
 METRIC = "decode queries/s and gathered-KV GB/s (% of HBM and tensor-pipe roofline)"
 UNIT = "queries/s"
 WORKLOAD = "c3"   # the headline workload; --workload selects another shape
-N_INDEX_SETS = 8
+N_INDEX_SETS = 8          # index sets of the isolated-step timing
 FLUSH_BYTES = 256 << 20
+MAX_LAYERS = 16
+GRAPH_STEPS = 128         # decode calls per captured graph (back-to-back timing)
+L2_TURNOVER = 3           # L2 capacities read between two reads of one layer
 # DRAM bytes (read + write) per launch of the dominant kernel on this workload, from
 # one ncu capture (profiles/fused_split_kernel_c3_b32_h64_k2048.md).  They describe the
 # kernel source they were taken on: with any other source the field is null.
@@ -182,7 +192,7 @@ def run_reference(args):
     w = W.WORKLOADS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     qbits, rows, remap = oracle_inputs(w, dev)
-    per_step_s = 2.0
+    per_step_s = min(2.0, 60.0 / max(1, args.steps))   # whole run about a minute or less
     time_oracle(qbits, rows, remap, w.softmax_scale, 0.0, max_queries=max(1, args.warmup))
     total_q, total_t, step_ms = 0, 0.0, []
     for _ in range(args.steps):
@@ -223,13 +233,26 @@ def job_throughput(world_size, batch, ms_per_step):
     return world_size * batch / (ms_per_step * 1e-3)
 
 
-def config_dict(w, S, fused=None):
-    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "topk": w.topk,
-            "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
-            "row_bytes": W.ROW_BYTES, "num_splits": S, "splits_merged_on_chip": fused,
-            "index_sets": N_INDEX_SETS,
-            "l2": "flushed between steps (256 MiB write) + 8 rotating index sets",
-            "timing": "CUDA-graph replays (one graph per index set), events around each replay"}
+def config_dict(w, S, fused=None, timing=None):
+    d = {"workload": w.name, "batch": w.batch, "heads": w.heads, "topk": w.topk,
+         "rows_per_seq": w.rows_per_seq, "index_law": w.index_law,
+         "row_bytes": W.ROW_BYTES, "num_splits": S, "splits_merged_on_chip": fused}
+    if timing:
+        d.update(timing)
+    return d
+
+
+def plan_layers(step_bytes: int, cache_bytes: int, l2_bytes: int, free_bytes: int) -> int:
+    """Number of layer caches for back-to-back timing, 0 when the data cannot exceed L2.
+
+    Between two reads of one layer, (NL - 1) other steps read at least L2_TURNOVER
+    L2 capacities; the caches together use at most 60 % of the free device memory.
+    """
+    need = -(-L2_TURNOVER * l2_bytes // max(step_bytes, 1)) + 1
+    nl = max(2, need)
+    if nl > MAX_LAYERS or nl * cache_bytes > 0.6 * free_bytes:
+        return 0
+    return nl
 
 
 def run_gpu(args):
@@ -260,75 +283,148 @@ def run_gpu(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        smla.sparse_mla_decode(q, kv, idx_sets[i % N_INDEX_SETS], w.softmax_scale, out=out,
-                               lse=lse, num_splits=S, workspace=wspace, stream=stream)
-        if not fused:
-            smla.sparse_mla_decode_split(q, kv, idx_sets[i % N_INDEX_SETS], S, w.softmax_scale,
-                                         o_part=o_part, lse_part=lse_part, stream=stream)
+    # ---- layers for back-to-back timing: each its own cache, q and index set ----
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    step_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
+    cache_bytes = kv.numel() * kv.element_size()
+    NL = plan_layers(int(step_bytes), cache_bytes, l2_bytes, torch.cuda.mem_get_info(dev)[0])
+    layers = []   # (q, kv, idx, idx_np)
+    for l in range(NL):
+        if l == 0:
+            layers.append((q, kv, idx_sets[0], idx_np[0]))
+            continue
+        lseed = seed + 104729 * l
+        li = W.make_indices(w, L, variant=1000 + l + 100 * rank)
+        layers.append((W.make_q(w, device=dev, gen_seed=lseed),
+                       W.make_cache(w, L, device=dev, gen_seed=lseed),
+                       torch.as_tensor(li, device=dev), li))
+    back_to_back = NL > 0
+
+    def decode(qq, kk, ii, **kw):
+        smla.sparse_mla_decode(qq, kk, ii, w.softmax_scale, out=out, lse=lse, num_splits=S,
+                               workspace=wspace, **kw)
+
+    def split_only(qq, kk, ii, **kw):
+        smla.sparse_mla_decode_split(qq, kk, ii, S, w.softmax_scale, o_part=o_part,
+                                     lse_part=lse_part, **kw)
 
     for i in range(args.warmup):
-        flush.zero_()
-        step(i)
+        if back_to_back:
+            decode(*layers[i % NL][:3], stream=stream)
+        else:
+            flush.zero_()
+            decode(q, kv, idx_sets[i % N_INDEX_SETS], stream=stream)
     torch.cuda.synchronize(dev)
     if smla.smla_device_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # One CUDA graph per index set holding the whole step (sparse_mla_decode: one
-    # clustered launch when the plan merges the splits on chip, else split + combine)
-    # and, when the step has two kernels, graphs of the split kernel alone for the
-    # roofline line.  Replays are timed with events on the launching stream; the L2
-    # flush runs outside the graphs, before each replay.
-    g_step, g_split = [], []
-    for i in range(N_INDEX_SETS):
+    def capture(fn, first, n):
+        """A CUDA graph of n consecutive steps starting at layer `first`."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            smla.sparse_mla_decode(q, kv, idx_sets[i], w.softmax_scale, out=out, lse=lse,
-                                   num_splits=S, workspace=wspace)
-        g_step.append(g)
-        if not fused:
+            for j in range(n):
+                fn(*layers[(first + j) % NL][:3])
+        return g
+
+    class BackToBack:
+        """Exactly K back-to-back steps as graph replays of G steps (+ a remainder)."""
+
+        def __init__(self, fn, K):
+            self.G = min(K, max(NL, (GRAPH_STEPS // NL) * NL))
+            self.K = K
+            self.full = capture(fn, 0, self.G)
+            rem = K % self.G
+            self.rem = capture(fn, 0, rem) if rem else None
+            self.full.replay()                 # untimed: first replay of the graphs
+            if self.rem is not None:
+                self.rem.replay()
+            torch.cuda.synchronize(dev)
+
+        def load(self, seconds):
+            """Untimed replays for about `seconds` (the clock sampler sees the load)."""
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < seconds:
+                for _ in range(8):
+                    self.full.replay()
+                torch.cuda.synchronize(dev)
+
+        def run(self):
+            """ms per step over exactly K steps, one event pair on the launching stream."""
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(self.K // self.G):
+                self.full.replay()
+            if self.rem is not None:
+                self.rem.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) / self.K
+
+    def time_isolated(fn, K):
+        """Mean ms of K single-step graph replays, L2 flushed before each."""
+        gs = []
+        for i in range(N_INDEX_SETS):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                smla.sparse_mla_decode_split(q, kv, idx_sets[i], S, w.softmax_scale,
-                                             o_part=o_part, lse_part=lse_part)
-            g_split.append(g)
-    for i in range(3):
-        flush.zero_()
-        g_step[i % N_INDEX_SETS].replay()
-        if g_split:
-            g_split[i % N_INDEX_SETS].replay()
-    torch.cuda.synchronize(dev)
+                fn(q, kv, idx_sets[i])
+            gs.append(g)
+        for i in range(3):
+            flush.zero_()
+            gs[i % N_INDEX_SETS].replay()
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            gs[i % N_INDEX_SETS].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if back_to_back:
+        b2b = BackToBack(decode, K)
+        # the dominant kernel: the fused step itself, or the split kernel of a
+        # two-kernel step timed on its own the same way
+        b2b_split = None if fused else BackToBack(split_only, K)
     sampler = ClockSampler(dev.index)
     sampler.start()
-    time.sleep(0.3)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    for i in range(K):
-        flush.zero_()
-        ev[i][0].record(stream)
-        g_step[i % N_INDEX_SETS].replay()
-        ev[i][1].record(stream)
-    for i in range(K if g_split else 0):
-        flush.zero_()
-        evs[i][0].record(stream)
-        g_split[i % N_INDEX_SETS].replay()
-        evs[i][1].record(stream)
+    if back_to_back:
+        b2b.load(0.6)
+        ms = b2b.run()
+        split_mean = ms if fused else b2b_split.run()
+    else:
+        ms = time_isolated(decode, K)
+        split_mean = ms if fused else time_isolated(split_only, K)
     torch.cuda.synchronize(dev)
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     if smla.smla_device_status() != 0:
         raise RuntimeError("device status set during the timed region")
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    # the dominant kernel: the fused step itself, or the split kernel of a two-kernel step
-    split_ms = [a.elapsed_time(b) for a, b in evs] if g_split else step_ms
-    ms = statistics.mean(step_ms)
-    split_mean = statistics.mean(split_ms)
+    iso_ms = time_isolated(decode, 20) if back_to_back else ms
+    if back_to_back:
+        timing = {"timing": f"back to back: CUDA-graph replays of {b2b.G} steps, one event "
+                            f"pair around all {K} steps; programmatic dependent launch "
+                            f"between steps; clocks sampled over 0.6 s of the same replays "
+                            f"just before and during the timed steps",
+                  "l2": f"inputs larger than L2: {NL} layers, each its own {cache_bytes / 1e9:.2f} GB "
+                        f"cache, q and index set; step i reads layer i mod {NL}, so "
+                        f"{(NL - 1) * step_bytes / 1e6:.0f} MB of other rows are read between two "
+                        f"reads of a layer (L2 {l2_bytes / 1e6:.0f} MB)",
+                  "layers": NL}
+    else:
+        timing = {"timing": "isolated steps: one single-step CUDA-graph replay per step, "
+                            "events around each",
+                  "l2": f"flushed before each step ({FLUSH_BYTES >> 20} MiB write); "
+                        f"{N_INDEX_SETS} rotating index sets (the workload's data cannot "
+                        f"exceed L2)",
+                  "layers": 1}
 
     # ---- context: the per-head fp32 SIMT form of the same step (the pages' pre-MMA
     # kernel style), on the same inputs, outside the timed region above ----
@@ -376,19 +472,20 @@ def run_gpu(args):
     e2e_value = job_throughput(ws, B, e2e_ms)
 
     hbm_peak, tc_peak, peak_kind = read_peaks()
-    mean_valid_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
+    timed_idx = [l[3] for l in layers] if back_to_back else idx_np
+    mean_valid_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in timed_idx)
     split_bytes = mean_valid_bytes + q.numel() * 2 + B * w.topk * 4
     if fused:   # the fused kernel also writes the final out and lse
         split_bytes += out.numel() * out.element_size() + lse.numel() * 4
     achieved = split_bytes / (split_mean * 1e-3) / 1e9
-    flops = statistics.mean(W.algorithmic_flops(w, i) for i in idx_np)
+    flops = statistics.mean(W.algorithmic_flops(w, i) for i in timed_idx)
     tc_achieved = flops / (split_mean * 1e-3) / 1e12
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w, S, fused),
+        "config": config_dict(w, S, fused, timing),
         "gathered_kv_gbs": ws * mean_valid_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
                      "kernel": "split_kernel (splits merged on chip)" if fused else "split_kernel",
@@ -405,7 +502,10 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": K * (1 if fused else 3),
-        "context": {"simt_ms_per_step": simt_ms, "tensor_core_speedup": simt_ms / ms,
+        "context": {"isolated_ms_per_step": iso_ms,
+                    "isolated": "one step alone: L2 flushed before it, events around a "
+                                "single-step graph replay (includes the whole launch latency)",
+                    "simt_ms_per_step": simt_ms, "tensor_core_speedup": simt_ms / iso_ms,
                     "simt": "sparse_mla_decode_simt: one CTA per (query, head), fp32, rows "
                             "re-read per head; 5 plain launches, L2 flushed"},
         "clocks": clocks,
@@ -413,7 +513,7 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         qb = W.bf16_bits(q)
         rows, remap = W.compact_rows(kv, idx_np[0])
-        del kv
+        del kv, layers
         n, el = time_oracle(qb, rows, remap, w.softmax_scale, args.cpu_seconds)
         line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
                                 "kind": "oracle",
@@ -429,7 +529,7 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "smla_internal.h"
+#include "smla_ptx.cuh"
 
 namespace smla {
 namespace {
@@ -50,6 +51,8 @@ __global__ void __launch_bounds__(kThreads)
     combine_few_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                        int BH, int S, __nv_bfloat162* __restrict__ out, float* __restrict__ lse) {
   const int t = threadIdx.x;
+  grid_dep_wait();   // the partials come from the previous kernel in the stream
+  grid_dep_launch();
   float l[P][SMAX];
   float2 v[P][SMAX];
 #pragma unroll
@@ -100,7 +103,8 @@ __global__ void __launch_bounds__(kThreads)
   const int t = threadIdx.x;
   const float* lp = lse_part + static_cast<int64_t>(pair) * S;
   const float2* op = reinterpret_cast<const float2*>(o_part) + static_cast<int64_t>(pair) * S * 224 + t;
-
+  grid_dep_wait();   // the partials come from the previous kernel in the stream
+  grid_dep_launch();
 
   float m = -INFINITY;
   for (int s = t; s < S; s += kThreads) m = fmaxf(m, lp[s]);
@@ -145,16 +149,17 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
   const int BH = B * H;
   if (BH == 0) return cudaSuccess;
   auto* o = static_cast<__nv_bfloat162*>(out);
-  if (S <= 2) {
-    combine_few_kernel<2, 16><<<(BH + 15) / 16, kThreads, 0, stream>>>(o_part, lse_part, BH, S, o, lse);
-  } else if (S <= 4) {
-    combine_few_kernel<4, 8><<<(BH + 7) / 8, kThreads, 0, stream>>>(o_part, lse_part, BH, S, o, lse);
-  } else if (S <= 8) {
-    combine_few_kernel<8, 4><<<(BH + 3) / 4, kThreads, 0, stream>>>(o_part, lse_part, BH, S, o, lse);
-  } else {
-    combine_kernel<<<BH, kThreads, 0, stream>>>(o_part, lse_part, S, o, lse);
-  }
-  return cudaGetLastError();
+  const dim3 blk(kThreads);
+  if (S <= 2)
+    return launch_programmatic(combine_few_kernel<2, 16>, dim3((BH + 15) / 16), blk, 0, stream,
+                               o_part, lse_part, BH, S, o, lse);
+  if (S <= 4)
+    return launch_programmatic(combine_few_kernel<4, 8>, dim3((BH + 7) / 8), blk, 0, stream,
+                               o_part, lse_part, BH, S, o, lse);
+  if (S <= 8)
+    return launch_programmatic(combine_few_kernel<8, 4>, dim3((BH + 3) / 4), blk, 0, stream,
+                               o_part, lse_part, BH, S, o, lse);
+  return launch_programmatic(combine_kernel, dim3(BH), blk, 0, stream, o_part, lse_part, S, o, lse);
 }
 
 }  // namespace smla

@@ -491,6 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *taddr_s;
+  // Nothing above touches global memory: under programmatic launch the previous
+  // kernel in the stream may run until here.
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tS = tmem;        // S^T: columns [0, NH)
   const uint32_t tO = tmem + NH;   // O^T block mb: columns [NH + mb*NH, NH + (mb+1)*NH)
 
@@ -1068,10 +1072,11 @@ cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices
   if (e != cudaSuccess) return e;
   const dim3 grid(S, H / NH, B);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
-  split_kernel<NH, kSplitOnly><<<grid, kThreads, C::kSmemBytes, stream>>>(
-      static_cast<const uint16_t*>(q), static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
-      nullptr, nullptr, H, topk, S, num_rows, stride, scale_log2);
-  return cudaGetLastError();
+  return launch_programmatic(split_kernel<NH, kSplitOnly>, grid, dim3(kThreads), C::kSmemBytes,
+                             stream, static_cast<const uint16_t*>(q),
+                             static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
+                             static_cast<__nv_bfloat16*>(nullptr), static_cast<float*>(nullptr), H,
+                             topk, S, num_rows, stride, scale_log2);
 }
 
 constexpr int kMaxClusterSplits = kMaxCluster;
@@ -1126,13 +1131,15 @@ cudaError_t launch_fused_t(const void* q, const void* kv, const int32_t* indices
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   bool fits = false;
   e = cluster_fits<NH, MODE>(dev, S, &fits);
   if (e != cudaSuccess) return e;

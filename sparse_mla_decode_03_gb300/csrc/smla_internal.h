@@ -12,6 +12,25 @@ constexpr int kRowBytes = 584;  // packed KV row
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCombineSplits = 1024;
 
+// Launches `kernel` with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel in the stream finishes.  Every kernel launched this way
+// calls grid_dep_wait before its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Launches the split kernel: grid (S, H / heads_per_cta, B), 640 threads.
 cudaError_t launch_split(const void* q, const void* kv, const int32_t* indices, float* o_part,
                          float* lse_part, int B, int H, int topk, int S, int64_t num_rows,

@@ -74,6 +74,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialization may start while the previous grid in the stream is still running;
+// grid_dep_wait returns once that grid has completed and its memory writes are
+// visible (at once when there is no such grid).  grid_dep_launch lets the next grid
+// be scheduled as soon as every CTA of this one has issued it or exited.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ---------------------------------------------------------------------------
 // Warp-wide.  Writes the allocated TMEM base address to shared memory at dst.

@@ -111,3 +111,38 @@ def test_on_chip_merge_matches_split_and_combine(H, S):
     assert_lse_close(lse_f.cpu().numpy(), ref_lse)
     assert_out_close(out_f.float().cpu().numpy(), out_u.float().cpu().numpy().astype(np.float64))
     assert np.all(out_f[2].float().cpu().numpy() == 0) and np.all(np.isneginf(lse_f[2].cpu().numpy()))
+
+
+@pytest.mark.parametrize("S", [4, 12])   # merged on chip / split + combine kernels
+def test_back_to_back_calls_keep_stream_order(S):
+    """Programmatic launch lets a call start while the previous kernel ends: each call
+    waits for it before touching memory.  A chain of calls sharing one workspace, each
+    reading a q written by the kernel just before it, must give bit for bit the
+    results of separate, synchronised calls."""
+    w, kv, q, idx_np = small_case(8, 64, 5000, 1000, seed=11)
+    idx = torch.as_tensor(idx_np, device="cuda")
+    p = make_params(8, 64, 1000, kv.shape[0], 584)
+    ws = torch.empty(smla_workspace_size(p, S), dtype=torch.uint8, device="cuda")
+    qs = [q * (1.0 + 0.25 * i) for i in range(4)]
+    ref = []
+    for qi in qs:
+        o, l = sparse_mla_decode(qi, kv, idx, num_splits=S, workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), l.clone()))
+    outs = [torch.empty((8, 64, 448), dtype=torch.bfloat16, device="cuda") for _ in qs]
+    lses = [torch.empty((8, 64), dtype=torch.float32, device="cuda") for _ in qs]
+    q_in = torch.empty_like(q)
+    for chained in (True, False):
+        for _ in range(3):
+            for o in outs:
+                o.zero_()
+            for i, qi in enumerate(qs):
+                if chained:
+                    q_in.copy_(qi)   # a kernel right before the call writes its input
+                # otherwise the calls follow each other directly, sharing the workspace
+                sparse_mla_decode(q_in if chained else qi, kv, idx, out=outs[i], lse=lses[i],
+                                  num_splits=S, workspace=ws)
+            torch.cuda.synchronize()
+            for i in range(len(qs)):
+                assert torch.equal(outs[i], ref[i][0])
+                assert torch.equal(lses[i], ref[i][1])
