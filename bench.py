@@ -56,8 +56,8 @@ L2_TURNOVER = 3           # L2 capacities read between two reads of one layer
 # one ncu capture (profiles/fused_split_kernel_c3_b32_h64_k2048.md).  They describe the
 # kernel source they were taken on: with any other source the field is null.
 TRAFFIC_KERNEL_SRC = "sparse_mla_decode_03_gb300/csrc/smla_decode.cu"
-TRAFFIC_SRC_SHA256_16 = "6a7812e6f4191ce7"
-TRAFFIC_BYTES = 47560192 + 479488
+TRAFFIC_SRC_SHA256_16 = "339159d03369e848"
+TRAFFIC_BYTES = 47559424 + 547328
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -289,6 +289,10 @@ def run_gpu(args):
     step_bytes = statistics.mean(W.gathered_kv_bytes(i) for i in idx_np)
     cache_bytes = kv.numel() * kv.element_size()
     NL = plan_layers(int(step_bytes), cache_bytes, l2_bytes, torch.cuda.mem_get_info(dev)[0])
+    if args.layers == 1:
+        NL = 0                      # one cache: isolated steps (small device footprint)
+    elif args.layers > 1:
+        NL = args.layers
     layers = []   # (q, kv, idx, idx_np)
     for l in range(NL):
         if l == 0:
@@ -534,6 +538,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer caches for back-to-back timing (0: enough to exceed L2 three "
+                         "times over; 1: one cache, isolated flushed steps)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS),
                     help="workload shape (default: the batch-32 headline workload)")
     args = ap.parse_args()
