@@ -50,3 +50,18 @@ def test_two_rank_aggregation_takes_the_max():
 def test_single_rank_is_identity():
     assert bench.aggregate_over_ranks([4.0, 5.0], torch.device("cpu"), 1) == [4.0, 5.0]
     assert bench.job_throughput(1, 32, 0.01) == 32 / 1e-5
+
+
+def test_layer_count_exceeds_l2_three_times_over():
+    """Back-to-back timing: between two reads of one layer, the other layers' rows
+    fill L2 at least three times; tiny steps or caches that do not fit fall back to
+    isolated steps (0)."""
+    l2, free = 136_000_000, 280 << 30    # the GB300 reports a 136 MB L2
+    step_c3, cache_c3 = 38_300_000, 1_224_736_768
+    nl = bench.plan_layers(step_c3, cache_c3, l2, free)
+    assert nl == 12
+    assert (nl - 1) * step_c3 >= bench.L2_TURNOVER * l2
+    assert (nl - 2) * step_c3 < bench.L2_TURNOVER * l2      # the smallest such count
+    assert bench.plan_layers(75_000, 10_000_000, l2, free) == 0          # batch-1 step
+    assert bench.plan_layers(step_c3, cache_c3, l2, 8 << 30) == 0        # no room
+    assert bench.plan_layers(500 << 20, 1 << 30, l2, free) == 2          # step > 3 x L2
