@@ -1,6 +1,7 @@
 // C ABI of libsmla.so: argument validation, split planning and kernel launches.
 // Declarations and their documentation are in include/smla.h.
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -55,8 +56,7 @@ int max_splits(const smla_params* p) {
 }
 
 // Plan: 1 CTA per SM is resident (the kernel uses ~210 KB of shared memory), so
-// choose S to minimise (waves of CTAs) x (128-token tiles per CTA + a fixed
-// per-CTA overhead of about a third of a tile), preferring fewer splits on ties.
+// choose S to minimise the modelled time below, preferring fewer splits on ties.
 int plan_splits(const smla_params* p, int sms) {
   const int groups = p->num_heads > 64 ? p->num_heads / 64 : 1;
   const int64_t ctas_per_split = static_cast<int64_t>(p->batch) * groups;
@@ -68,7 +68,14 @@ int plan_splits(const smla_params* p, int sms) {
     const int gmax = (granules + s - 1) / s;              // granules of the largest split
     const int tiles = (gmax * 16 + 127) / 128;
     const int64_t waves = (ctas_per_split * s + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (tiles + 0.35);
+    // In units of one steady-state 128-slot tile: the tiles of the largest split, the
+    // fixed prologue and epilogue, and the gather of the first tile's rows, which a
+    // CTA waits for in full before its first tile starts (measured: a full first tile
+    // costs ~0.8 tile more than a nearly empty one).  Beyond the cluster size the
+    // splits are merged by a second kernel.
+    const int first_rows = std::min(gmax * 16, 128);
+    const double cost = static_cast<double>(waves) * (tiles + 0.35 + 0.8 * first_rows / 128.0) +
+                        (s > 8 ? 0.6 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
