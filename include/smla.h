@@ -32,6 +32,15 @@
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).  They do not
  *     synchronise the host and allocate nothing, so they may be captured in a CUDA
  *     graph once the device has been initialised by one eager call.
+ *   - The decode and combine kernels are launched with programmatic stream
+ *     serialization (programmatic dependent launch): a kernel may be scheduled
+ *     while the previous kernel in the stream is still running, and it waits for
+ *     that kernel to complete (griddepcontrol.wait) before its first access to
+ *     global memory, so stream order holds for every input, output and workspace
+ *     byte.  The kernels also allow the next kernel in the stream to be scheduled
+ *     early; a caller's kernel launched with the same attribute must wait the same
+ *     way before it reads this library's outputs (one launched without it simply
+ *     waits for completion).
  *   - Layouts are dense, row-major, with the shapes given.  bf16 means IEEE
  *     bfloat16 bit patterns (uint16).
  *   - Return value: SMLA_OK (0) or a negative smla_status.  Argument errors are
