@@ -612,7 +612,7 @@ def run_gpu(args):
                             "re-read per head; 5 plain launches, L2 flushed"},
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:   # the oracle baseline: N = 1 only
         qb = W.bf16_bits(q)
         rows, remap = W.compact_rows(kv, idx_np[0])
         del kv, layers
