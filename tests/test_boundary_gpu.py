@@ -146,3 +146,75 @@ def test_back_to_back_calls_keep_stream_order(S):
             for i in range(len(qs)):
                 assert torch.equal(outs[i], ref[i][0])
                 assert torch.equal(lses[i], ref[i][1])
+
+
+@pytest.mark.parametrize("capture", [False, True])
+def test_pipelined_host_copies_over_three_streams(capture):
+    """The serving pattern the bench's end-to-end leg uses: inputs copied from pinned
+    host memory on one stream, decode on another, results copied back on a third,
+    three rotating device buffer sets, optionally captured in a CUDA graph.  Every
+    step's host result must equal a separate synchronous call bit for bit."""
+    w, kv, q, idx_np = small_case(4, 64, 3000, 700, seed=21)
+    idx = torch.as_tensor(idx_np, device="cuda")
+    p = make_params(4, 64, 700, kv.shape[0], 584)
+    S = smla_default_num_splits(p)
+    ws = torch.empty(smla_workspace_size(p, S), dtype=torch.uint8, device="cuda")
+    n_src, NB, n = 5, 3, 15
+    qs = [q * (1.0 + 0.125 * i) for i in range(n_src)]
+    ref = []
+    for qi in qs:
+        o, l = sparse_mla_decode(qi, kv, idx, num_splits=S, workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((o.cpu(), l.cpu()))
+    q_h = [x.cpu().pin_memory() for x in qs]
+    idx_h = idx.cpu().pin_memory()
+    q_d = [torch.empty_like(q) for _ in range(NB)]
+    idx_d = [torch.empty_like(idx) for _ in range(NB)]
+    out_d = [torch.empty((4, 64, 448), dtype=torch.bfloat16, device="cuda") for _ in range(NB)]
+    lse_d = [torch.empty((4, 64), dtype=torch.float32, device="cuda") for _ in range(NB)]
+    out_h = [torch.empty((4, 64, 448), dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    lse_h = [torch.empty((4, 64), dtype=torch.float32).pin_memory() for _ in range(n)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(NB)]
+    ev_dec = [torch.cuda.Event() for _ in range(NB)]
+    ev_res = [torch.cuda.Event() for _ in range(NB)]
+
+    def steps(cs, chained):
+        for i in range(n):
+            k = i % NB
+            if chained or i >= NB:
+                s_in.wait_event(ev_dec[k])
+            with torch.cuda.stream(s_in):
+                q_d[k].copy_(q_h[i % n_src], non_blocking=True)
+                idx_d[k].copy_(idx_h, non_blocking=True)
+            ev_in[k].record(s_in)
+            cs.wait_event(ev_in[k])
+            if chained or i >= NB:
+                cs.wait_event(ev_res[k])
+            sparse_mla_decode(q_d[k], kv, idx_d[k], out=out_d[k], lse=lse_d[k], num_splits=S,
+                              workspace=ws, stream=cs)
+            ev_dec[k].record(cs)
+            s_out.wait_event(ev_dec[k])
+            with torch.cuda.stream(s_out):
+                out_h[i].copy_(out_d[k], non_blocking=True)
+                lse_h[i].copy_(lse_d[k], non_blocking=True)
+            ev_res[k].record(s_out)
+
+    if capture:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            s_in.wait_stream(cs)
+            s_out.wait_stream(cs)
+            steps(cs, chained=False)
+            cs.wait_stream(s_in)
+            cs.wait_stream(s_out)
+        for h in out_h:
+            h.zero_()
+        g.replay()
+    else:
+        steps(torch.cuda.current_stream(), chained=True)
+    torch.cuda.synchronize()
+    for i in range(n):
+        assert torch.equal(out_h[i], ref[i % n_src][0])
+        assert torch.equal(lse_h[i], ref[i % n_src][1])
