@@ -191,3 +191,17 @@ def test_workload_parity(key):
     assert_lse_close(lse[sel], rl)
     del kv
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# the largest accepted top-k: every row of a 65536-row sequence selected
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("S", [0, 8])   # default plan (split + combine kernels) / cluster merge
+def test_maximum_topk_every_row(S):
+    w, kv, q, idx_np = small_case(1, 64, 65536, 65536, seed=31)
+    assert idx_np.shape == (1, 65536) and np.array_equal(np.sort(idx_np[0]), np.arange(65536))
+    out, lse = _run(q, kv, idx_np, num_splits=S)
+    ro, rl = oracle_decode(q, kv, idx_np)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+    assert smla_device_status() == 0
