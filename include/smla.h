@@ -64,7 +64,7 @@ typedef struct CUstream_st* smla_stream_t; /* == cudaStream_t */
 enum smla_status {
   SMLA_OK = 0,
   SMLA_ERR_INVALID_ARG = -1,        /* null pointer, bad alignment, bad size          */
-  SMLA_ERR_UNSUPPORTED_SHAPE = -2,  /* num_heads not in {16, 32, 64, 128}, ...        */
+  SMLA_ERR_UNSUPPORTED_SHAPE = -2,  /* num_heads not in {16, 32, 64, 128}, batch > 65535, ... */
   SMLA_ERR_WORKSPACE_TOO_SMALL = -3,
   SMLA_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
   SMLA_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed           */
@@ -78,7 +78,7 @@ enum smla_status {
 
 /* Problem description shared by the entry points. */
 typedef struct smla_params {
-  int32_t batch;          /* B: decode queries (one token each), >= 1                  */
+  int32_t batch;          /* B: decode queries (one token each), 1 .. 65535            */
   int32_t num_heads;      /* H: query heads, one of 16, 32, 64, 128                    */
   int32_t topk;           /* k: index slots per query, 1 .. 65536                      */
   int32_t reserved;       /* must be 0                                                 */

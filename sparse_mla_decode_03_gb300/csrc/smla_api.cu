@@ -47,6 +47,7 @@ int check_params(const smla_params* p) {
     return SMLA_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<int64_t>(p->batch) * p->num_heads > (int64_t(1) << 30))
     return SMLA_ERR_UNSUPPORTED_SHAPE;
+  if (p->batch > 65535) return SMLA_ERR_UNSUPPORTED_SHAPE;   // grid z of the decode kernels
   return SMLA_OK;
 }
 

@@ -58,6 +58,7 @@ def test_workspace_size_arithmetic(lib):
     ("num_heads", 48, _lib.SMLA_ERR_UNSUPPORTED_SHAPE),
     ("num_heads", 256, _lib.SMLA_ERR_UNSUPPORTED_SHAPE),
     ("batch", 0, _lib.SMLA_ERR_INVALID_ARG),
+    ("batch", 65536, _lib.SMLA_ERR_UNSUPPORTED_SHAPE),
     ("topk", 0, _lib.SMLA_ERR_INVALID_ARG),
     ("kv_row_stride", 580, _lib.SMLA_ERR_INVALID_ARG),
     ("kv_row_stride", 588, _lib.SMLA_ERR_INVALID_ARG),
