@@ -53,7 +53,7 @@ MAX_LAYERS = 16
 GRAPH_STEPS = 128         # decode calls per captured graph (back-to-back timing)
 L2_TURNOVER = 3           # L2 capacities read between two reads of one layer
 # DRAM bytes (read + write) per launch of the dominant kernel on this workload, from
-# one ncu capture (profiles/fused_split_kernel_c3_b32_h64_k2048.md).  They describe the
+# one ncu capture of the decode kernel on the batch-32 workload.  They describe the
 # kernel source they were taken on: with any other source the field is null.
 TRAFFIC_KERNEL_SRC = "sparse_mla_decode_03_gb300/csrc/smla_decode.cu"
 TRAFFIC_SRC_SHA256_16 = "339159d03369e848"
@@ -185,6 +185,58 @@ def cores_used() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """CPU model name of the host (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+SINGLE_THREAD_ENV = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                       "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS")}
+
+
+def oracle_child(path: str, seconds: float) -> None:
+    """Child process of the single-core baseline: pinned to one core, one BLAS thread
+    (set in its environment before numpy loads), times the oracle on the saved inputs
+    and prints {"queries": n, "seconds": t}."""
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except Exception:
+        pass
+    d = np.load(path)
+    n, el = time_oracle(d["q"], d["rows"], d["remap"], float(d["scale"]), seconds)
+    print(json.dumps({"queries": n, "seconds": el, "cores": cores_used()}), flush=True)
+
+
+def time_oracle_single_core(qbits, rows, remap, scale, seconds):
+    """The oracle on one pinned core with one BLAS thread, in a child process."""
+    import tempfile
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "oracle_inputs.npz")
+        np.savez(path, q=qbits, rows=rows, remap=remap, scale=np.float64(scale))
+        env = dict(os.environ, **SINGLE_THREAD_ENV)
+        p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", path,
+                            "--cpu-seconds", str(seconds)], capture_output=True, text=True,
+                           env=env, timeout=600)
+        if p.returncode != 0:
+            return None
+        return json.loads(p.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
@@ -208,6 +260,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w, None),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{total_q} queries of the workload, about {per_step_s:.0f} s "
                                    f"of oracle work per step, one query per call"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -617,10 +670,17 @@ def run_gpu(args):
         rows, remap = W.compact_rows(kv, idx_np[0])
         del kv, layers
         n, el = time_oracle(qb, rows, remap, w.softmax_scale, args.cpu_seconds)
+        one = time_oracle_single_core(qb, rows, remap, w.softmax_scale, args.cpu_seconds / 2)
         line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": cpu_model(),
                                 "sample": f"{n} queries of the same workload (cycling over the "
-                                          f"batch of {B}), {el:.1f} s, numpy float64"}
+                                          f"batch of {B}), {el:.1f} s, numpy float64, all "
+                                          f"host cores",
+                                "single_core": None if one is None else {
+                                    "value": one["queries"] / one["seconds"], "unit": UNIT,
+                                    "cores": one["cores"],
+                                    "sample": f"{one['queries']} queries, {one['seconds']:.1f} s, "
+                                              f"pinned to one core, one BLAS thread"}}
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -641,7 +701,11 @@ def main():
                          "times over; 1: one cache, isolated flushed steps)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS),
                     help="workload shape (default: the batch-32 headline workload)")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args.oracle_child, args.cpu_seconds)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -198,9 +198,13 @@ int sparse_mla_decode_simt(const void* q, const void* kv_cache, const int32_t* i
  *     num_splits whose partials do not fit, or a problem for which even one split
  *     does not fit (batch * num_heads above about 9300), returns
  *     SMLA_ERR_SCRATCH_TOO_SMALL before anything is launched.
+ *   - It runs the same kernels as sparse_mla_decode with the resolved split count
+ *     (one clustered launch that also merges the splits, or split + combine).
  *   - The first call on each device looks up the scratch array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before
- *     any stream capture on the device.
+ *     (cudaGetSymbolAddress) with that device current and caches it; make that first
+ *     call before any stream capture on the device.  The cached address does not
+ *     survive cudaDeviceReset: a call that fails with SMLA_ERR_CUDA drops it, and
+ *     the next call looks it up again.  The cache is guarded by a mutex.
  *   - All calls in the process share the one scratch array, which keeps the last
  *     call's partials (every partial a call reads is written by the same call, so
  *     nothing needs clearing).  Calls whose kernels overlap on the GPU (several

@@ -2,6 +2,7 @@
 // Declarations and their documentation are in include/smla.h.
 #include <cmath>
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -14,23 +15,27 @@ using smla::kMaxCombineSplits;
 using smla::kMaxSplits;
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices] = {0};  // 0 = not queried yet, -1 = unsupported device
+// 0 = not queried yet, -1 = unsupported device, else the SM count.  Written at most
+// once per device with the same value by whichever host thread gets there first.
+std::atomic<int> g_sm_count[kMaxDevices];
 
 // SM count of the current device, or an error status if it is not sm_103.
 int current_device_sms(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SMLA_ERR_UNSUPPORTED_DEVICE;
-  if (g_sm_count[dev] == 0) {
+  int v = g_sm_count[dev].load(std::memory_order_acquire);
+  if (v == 0) {
     int major = 0, minor = 0, n = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SMLA_ERR_CUDA;
-    g_sm_count[dev] = (major == 10 && minor == 3) ? n : -1;
+    v = (major == 10 && minor == 3) ? n : -1;
+    g_sm_count[dev].store(v, std::memory_order_release);
   }
-  if (g_sm_count[dev] < 0) return SMLA_ERR_UNSUPPORTED_DEVICE;
-  *sms = g_sm_count[dev];
+  if (v < 0) return SMLA_ERR_UNSUPPORTED_DEVICE;
+  *sms = v;
   return SMLA_OK;
 }
 
@@ -87,23 +92,59 @@ int plan_splits(const smla_params* p, int sms) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+}  // namespace
+
+namespace smla {
+
+int check_device() {
+  int sms = 0;
+  return current_device_sms(&sms);
+}
+
+// One whole decode step on validated arguments: one launch when the splits of a
+// query fit in a thread-block cluster (they merge their partials in the workspace
+// inside that launch), split + combine kernels otherwise.
+int launch_step(const void* q, const void* kv_cache, const int32_t* indices, void* out,
+                float* lse, const smla_params* p, int S, void* workspace, cudaStream_t s) {
+  const size_t bhs = static_cast<size_t>(p->batch) * p->num_heads * S;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             round256(bhs * kNope * sizeof(float)));
+  cudaError_t e = launch_decode_fused(q, kv_cache, indices, o_part, lse_part, out, lse,
+                                      p->batch, p->num_heads, p->topk, S, p->num_rows,
+                                      p->kv_row_stride, p->softmax_scale, s);
+  if (e == cudaSuccess) return SMLA_OK;
+  if (e != cudaErrorNotSupported) return SMLA_ERR_CUDA;
+  e = launch_split(q, kv_cache, indices, o_part, lse_part, p->batch, p->num_heads, p->topk, S,
+                   p->num_rows, p->kv_row_stride, p->softmax_scale, s);
+  if (e != cudaSuccess) return SMLA_ERR_CUDA;
+  e = launch_combine(o_part, lse_part, p->batch, p->num_heads, S, out, lse, s);
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+}  // namespace smla
+
+namespace {
+
 void workspace_layout(const smla_params* p, int S, size_t* o_bytes, size_t* total) {
   const size_t bhs = static_cast<size_t>(p->batch) * p->num_heads * S;
   *o_bytes = round256(bhs * smla::kNope * sizeof(float));
   *total = *o_bytes + round256(bhs * sizeof(float));
 }
 
+// The split count of a call: the plan for the current device (requested = 0, which
+// needs an sm_103 GPU to be current) or the caller's count (pure arithmetic).
 int resolve_splits(const smla_params* p, int32_t requested, int* S) {
   if (requested < 0) return SMLA_ERR_INVALID_ARG;
-  if (requested == 0) {
-    int sms = 0;
-    const int st = current_device_sms(&sms);
-    if (st != SMLA_OK) return st;
-    *S = plan_splits(p, sms);
+  if (requested > max_splits(p)) return SMLA_ERR_INVALID_ARG;
+  if (requested > 0) {
+    *S = requested;
     return SMLA_OK;
   }
-  if (requested > max_splits(p)) return SMLA_ERR_INVALID_ARG;
-  *S = requested;
+  int sms = 0;
+  const int st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  *S = plan_splits(p, sms);
   return SMLA_OK;
 }
 
@@ -210,22 +251,11 @@ int sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* indice
   workspace_layout(p, S, &o_bytes, &total);
   if (workspace == nullptr || !aligned(workspace, 256)) return SMLA_ERR_INVALID_ARG;
   if (workspace_bytes < total) return SMLA_ERR_WORKSPACE_TOO_SMALL;
-  float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // One launch when the splits of a query fit in a thread-block cluster (they merge
-  // their partials in the workspace inside that launch); split + combine otherwise.
-  cudaError_t e = smla::launch_decode_fused(q, kv_cache, indices, o_part, lse_part, out, lse,
-                                            p->batch, p->num_heads, p->topk, S, p->num_rows,
-                                            p->kv_row_stride, p->softmax_scale, s);
-  if (e == cudaSuccess) return SMLA_OK;
-  if (e != cudaErrorNotSupported) return SMLA_ERR_CUDA;
-  e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
-                                     p->num_heads, p->topk, S, p->num_rows, p->kv_row_stride,
-                                     p->softmax_scale, s);
-  if (e != cudaSuccess) return SMLA_ERR_CUDA;
-  e = smla::launch_combine(o_part, lse_part, p->batch, p->num_heads, S, out, lse, s);
-  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  int sms = 0;
+  st = current_device_sms(&sms);    // an explicit split count skips the plan's check
+  if (st != SMLA_OK) return st;
+  return smla::launch_step(q, kv_cache, indices, out, lse, p, S, workspace,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 int smla_paged_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes) {
@@ -255,6 +285,9 @@ int sparse_mla_decode_paged(const void* q, const void* kv_pages, const int32_t* 
   st = smla_paged_workspace_size(p, num_splits, &need);
   if (st != SMLA_OK) return st;
   if (workspace_bytes < need) return SMLA_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
   // the translated rows sit after the decode's own part of the workspace
   int32_t* rows = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + total);
   const cudaError_t e = smla::launch_paged_rows(indices, block_table, p->batch, p->topk,

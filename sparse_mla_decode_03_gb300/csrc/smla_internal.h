@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/smla.h"
+
 namespace smla {
 
 constexpr int kQkDim = 512;     // q / k width: 448 nope + 64 rope
@@ -62,6 +64,16 @@ cudaError_t launch_simt(const void* q, const void* kv, const int32_t* indices, v
 cudaError_t launch_paged_rows(const int32_t* indices, const int32_t* block_table, int B, int topk,
                               int max_pages, int page_size, int64_t num_rows, int32_t* rows,
                               cudaStream_t stream);
+
+// SMLA_OK if the current device is a compute capability 10.3 GPU, else an
+// smla_status (SMLA_ERR_UNSUPPORTED_DEVICE or SMLA_ERR_CUDA).
+int check_device();
+
+// One whole decode step (sparse_mla_decode after argument checks): S splits, the
+// split partials in `workspace` (laid out as smla_workspace_size describes).
+// Returns an smla_status.
+int launch_step(const void* q, const void* kv_cache, const int32_t* indices, void* out,
+                float* lse, const smla_params* p, int S, void* workspace, cudaStream_t stream);
 
 // Device address of the status word (kernels in other translation units record
 // their errors through it; device variables are not shared across them).

@@ -1,7 +1,8 @@
-// sparse_mla_decode_noalloc: the whole decode step (split + combine) with the split
-// partials kept in a fixed scratch array that belongs to the library, for callers
+// sparse_mla_decode_noalloc: the whole decode step with the split partials kept in a
+// fixed scratch array that belongs to the library, for callers
 // that cannot allocate device memory.  Declared and documented in include/smla.h.
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/smla.h"
 #include "smla_internal.h"
@@ -15,17 +16,14 @@ constexpr size_t kScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;                       // guards g_scratch_ptr
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Device address of the scratch array on the current device.  The host-side name
 // g_noalloc_scratch is only a stand-in for the symbol, so the address is looked
 // up once per device (with that device current) and cached.
-int scratch_address(void** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SMLA_ERR_UNSUPPORTED_DEVICE;
+int scratch_address(int dev, void** ptr) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
@@ -34,6 +32,13 @@ int scratch_address(void** ptr) {
   }
   *ptr = g_scratch_ptr[dev];
   return SMLA_OK;
+}
+
+// Forgets the cached address of a device (after a CUDA error, which may come from a
+// reset device whose module, and with it the scratch, was reloaded elsewhere).
+void forget_scratch_address(int dev) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  g_scratch_ptr[dev] = nullptr;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -64,18 +69,18 @@ extern "C" int sparse_mla_decode_noalloc(const void* q, const void* kv_cache,
   st = smla_workspace_size(p, S, &need);
   if (st != SMLA_OK) return st;
   if (need > kScratchBytes) return SMLA_ERR_SCRATCH_TOO_SMALL;
-  void* scratch = nullptr;
-  st = scratch_address(&scratch);
+  st = smla::check_device();
   if (st != SMLA_OK) return st;
-  const size_t bhs = static_cast<size_t>(p->batch) * p->num_heads * S;
-  float* o_part = static_cast<float*>(scratch);
-  float* lse_part =
-      reinterpret_cast<float*>(static_cast<char*>(scratch) + round256(bhs * smla::kNope * 4));
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = smla::launch_split(q, kv_cache, indices, o_part, lse_part, p->batch,
-                                     p->num_heads, p->topk, S, p->num_rows, p->kv_row_stride,
-                                     p->softmax_scale, s);
-  if (e != cudaSuccess) return SMLA_ERR_CUDA;
-  e = smla::launch_combine(o_part, lse_part, p->batch, p->num_heads, S, out, lse, s);
-  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SMLA_ERR_UNSUPPORTED_DEVICE;
+  void* scratch = nullptr;
+  st = scratch_address(dev, &scratch);
+  if (st != SMLA_OK) return st;
+  // the same launches as sparse_mla_decode with this split count, the scratch as
+  // its workspace
+  st = smla::launch_step(q, kv_cache, indices, out, lse, p, S, scratch,
+                         reinterpret_cast<cudaStream_t>(stream));
+  if (st == SMLA_ERR_CUDA) forget_scratch_address(dev);
+  return st;
 }

@@ -14,11 +14,15 @@ SCALE = 1.0 / math.sqrt(512)
 
 # Parity bar.  fp32 LSE within 1e-3 absolute.  bf16 output within 1e-2 absolute
 # everywhere the outputs are O(1) (strict_abs).  Where |out| >> 1 (the x50-outlier
-# workload) no bf16 result can be within 1e-2, so the bound adds the bf16 rounding
-# of the output (2^-8 |ref|) and of the attention weights that feed the bf16 PV
-# product (2^-8 D, D = sum_t w_t |v_t - ref|, see oracle.weighted_deviation).
+# workload) no bf16 result can be within 1e-2, so the bound adds the two roundings
+# the kernel's arithmetic makes, each with a factor-2 allowance:
+#   - the output rounded to bf16: half an ulp is 2^-9 |ref|, allowed 2^-8 |ref|;
+#   - the attention weights rounded to f16 before the tensor-core PV product: a
+#     relative eps <= 2^-11 per weight moves the normalised output by at most
+#     eps * D, D = sum_t w_t |v_t - ref| (oracle.weighted_deviation), allowed 2^-10 D.
 OUT_ABS = 1e-2
 OUT_REL = 2.0 ** -8
+P_REL = 2.0 ** -10
 LSE_ABS = 1e-3
 
 
@@ -28,7 +32,7 @@ def assert_out_close(gpu_out: np.ndarray, ref: np.ndarray, strict_abs: bool = Tr
     assert np.all(np.isfinite(gpu_out)), "non-finite output"
     bound = OUT_ABS + OUT_REL * np.abs(ref)
     if D is not None:
-        bound = bound + OUT_REL * D
+        bound = bound + P_REL * D
     bad = err > bound
     assert not bad.any(), (
         f"out mismatch at {np.argwhere(bad)[:5].tolist()}: max err {err.max():.3g}, "

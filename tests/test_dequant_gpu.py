@@ -1,0 +1,134 @@
+"""Parity of the kernel's dequantisation over the whole UE8M0 scale range, and its
+f16-range report.
+
+Rows follow the format of "The Power-of-Two Trap: Debugging a Triton MMA Kernel on
+Blackwell GPUs", sections "3. The Scale Indexing Complication" and "Input Knowledge
+Required": 448 FP8 e4m3 values, one UE8M0 scale byte 2^(s - 127) per 64-column group.
+The benchmark workloads quantise N(0, 1) data, so their scale bytes sit near 120..126.
+Real caches also hold groups of very small magnitude (scale bytes far below 127, where
+2^(s - 127) is an f16 subnormal or below the f16 range) and groups with large scales.
+These tests build rows whose scale bytes are spread over 100..142, with rows whose
+scales are all ordinary, rows with a single unusual group and rows with every group
+drawn from the whole range, at both 8-byte alignments of a 584-byte row, and compare
+the decode with the oracle element by element.  A value beyond the f16 range must set
+SMLA_ERR_RANGE in the device status word."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_mla_decode_03_gb300 import _lib, sparse_mla_decode, smla_device_status
+from sparse_mla_decode_03_gb300 import workloads as W
+
+from _helpers import SCALE, assert_lse_close, assert_out_close, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+ORDINARY = np.arange(113, 135)                     # scale bytes the workloads produce
+UNUSUAL = np.concatenate([np.arange(100, 113), np.arange(135, 143)])
+
+
+def _e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round x to e4m3 (RNE, saturated to +-448) and return the bytes."""
+    t = torch.as_tensor(np.clip(x, -448.0, 448.0), dtype=torch.float32)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def build_rows(n: int, seed: int, magnitude: float = 1.0) -> np.ndarray:
+    """n packed rows whose group scales cover 100..142.
+
+    Per row a pattern: 40 % all groups ordinary, 30 % one unusual group, 30 % every
+    group drawn from 100..142.  Group values are N(0, magnitude) written with the
+    group's own scale byte s (x / 2^(s-127) rounded to e4m3 and saturated), so the
+    dequantised magnitudes stay O(magnitude) whatever s is; for the smallest scales
+    the codes saturate and the values are tiny."""
+    rng = np.random.default_rng(seed)
+    rows = np.zeros((n, W.ROW_BYTES), dtype=np.uint8)
+    for r in range(n):
+        kind = rng.random()
+        s = rng.choice(ORDINARY, size=W.N_GROUPS)
+        if kind >= 0.4 and kind < 0.7:
+            s[rng.integers(W.N_GROUPS)] = rng.choice(UNUSUAL)
+        elif kind >= 0.7:
+            s = rng.integers(100, 143, size=W.N_GROUPS)
+        x = rng.standard_normal(W.NOPE) * magnitude
+        scale = np.ldexp(1.0, s.astype(np.int64) - 127)
+        codes = _e4m3_codes(x / np.repeat(scale, W.GROUP))
+        rows[r, :W.NOPE] = codes
+        rows[r, W.SCALE_OFF:W.SCALE_OFF + W.N_GROUPS] = s
+        rows[r, W.PAD_OFF] = rng.integers(256)
+        rope = torch.as_tensor(rng.standard_normal(W.ROPE), dtype=torch.float32)
+        rows[r, W.ROPE_OFF:] = rope.to(torch.bfloat16).view(torch.uint8).numpy()
+    return rows
+
+
+def _decode(q, kv, idx_np, **kw):
+    idx = torch.as_tensor(np.ascontiguousarray(idx_np), dtype=torch.int32, device="cuda")
+    out, lse = sparse_mla_decode(q, kv, idx, **kw)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("H", [16, 64])
+def test_scale_bytes_over_the_whole_range(H):
+    rows = build_rows(900, seed=50 + H)
+    kv = torch.as_tensor(rows, device="cuda")
+    B, k = 3, 300
+    rng = np.random.default_rng(H)
+    idx = np.stack([rng.choice(rows.shape[0], size=k, replace=False) for _ in range(B)])
+    idx = idx.astype(np.int32)
+    assert (idx % 2 == 0).any() and (idx % 2 == 1).any()      # both 8-byte row shifts
+    q = (torch.randn((B, H, 512), generator=torch.Generator().manual_seed(H))
+         .to(torch.bfloat16).cuda())
+    smla_device_status(clear=True)
+    out, lse = _decode(q, kv, idx)
+    assert smla_device_status() == 0
+    ro, rl = oracle_decode(q, kv, idx, scale=SCALE)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_every_group_of_a_row_unusual_at_once():
+    """All rows in the index list have only unusual scale bytes (every converting
+    lane takes the checked path), including the smallest groups that vanish in f16."""
+    rng = np.random.default_rng(5)
+    rows = build_rows(256, seed=6)
+    for r in range(rows.shape[0]):
+        rows[r, W.SCALE_OFF:W.SCALE_OFF + W.N_GROUPS] = rng.choice(UNUSUAL, size=W.N_GROUPS)
+    kv = torch.as_tensor(rows, device="cuda")
+    idx = rng.permutation(256)[None, :200].astype(np.int32)
+    q = torch.randn((1, 64, 512), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
+    smla_device_status(clear=True)
+    out, lse = _decode(q, kv, idx)
+    assert smla_device_status() == 0
+    ro, rl = oracle_decode(q, kv, idx, scale=SCALE)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_value_beyond_f16_range_is_reported():
+    rows = build_rows(200, seed=7)
+    rows[11, 200] = 0x7E                                  # e4m3 448 in group 3
+    rows[11, W.SCALE_OFF + 3] = 142                       # x 2^15 > 65504
+    kv = torch.as_tensor(rows, device="cuda")
+    idx = np.array([[11, 3, 4, 5], [6, 7, 8, 9]], dtype=np.int32)
+    q = torch.randn((2, 64, 512), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).cuda()
+    smla_device_status(clear=True)
+    out, lse = _decode(q, kv, idx)
+    assert smla_device_status(clear=True) == _lib.SMLA_ERR_RANGE
+    # the query that never reads the row is unaffected
+    ro, rl = oracle_decode(q, kv, idx, scale=SCALE, queries=[1])
+    assert_out_close(out[1:], ro)
+    assert_lse_close(lse[1:], rl)
+    assert smla_device_status() == 0
+
+
+def test_q_beyond_f16_range_is_reported():
+    rows = build_rows(64, seed=8)
+    kv = torch.as_tensor(rows, device="cuda")
+    idx = np.arange(32, dtype=np.int32)[None]
+    q = torch.zeros((1, 16, 512), dtype=torch.float32)
+    q[0, 3, 10] = 1.0e6                                   # bf16 holds it, f16 does not
+    smla_device_status(clear=True)
+    _decode(q.to(torch.bfloat16).cuda(), kv, idx)
+    assert smla_device_status(clear=True) == _lib.SMLA_ERR_RANGE
+    assert smla_device_status() == 0

@@ -60,3 +60,35 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     # 128 x 128 heads x 448 fp32 partials = 28 MiB even with one split
     assert _noalloc(q, kv, idx, out, lse) == _lib.SMLA_ERR_SCRATCH_TOO_SMALL
     assert _noalloc(q, kv, idx, out, lse, num_splits=2) == _lib.SMLA_ERR_SCRATCH_TOO_SMALL
+
+
+def test_noalloc_lowers_the_split_count_until_the_partials_fit():
+    """When the default plan's partials exceed the 16 MiB scratch but fewer splits fit,
+    the call takes the largest split count that fits; its result is then bit for bit
+    that of sparse_mla_decode with that split count and a caller workspace."""
+    from sparse_mla_decode_03_gb300 import smla_default_num_splits, smla_workspace_size
+    limit = 16 << 20
+    rows_per_seq = 4096
+    for B, H, k in [(19, 64, 2048), (25, 64, 2048), (37, 64, 2048), (49, 64, 2048),
+                    (37, 128, 2048), (26, 128, 4096)]:
+        p = make_params(B, H, k, B * rows_per_seq, 584)
+        S0 = smla_default_num_splits(p)
+        if smla_workspace_size(p, S0) > limit and smla_workspace_size(p, 1) <= limit:
+            break
+    else:
+        pytest.fail("no candidate shape whose default plan exceeds the scratch")
+    S = S0
+    while S > 1 and smla_workspace_size(p, S) > limit:
+        S -= 1
+    assert 1 <= S < S0
+    w = W.Workload("noalloc_fit", B, H, k, rows_per_seq, "uniform", seed=78)
+    L = W.seq_lengths(w)
+    kv = W.make_cache(w, L, device="cuda")
+    q = W.make_q(w, device="cuda")
+    idx = torch.as_tensor(W.make_indices(w, L), device="cuda")
+    out = torch.empty((B, H, 448), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    assert _noalloc(q, kv, idx, out, lse) == 0
+    ref_out, ref_lse = sparse_mla_decode(q, kv, idx, num_splits=S)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
