@@ -33,12 +33,12 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
 
-def build_rows(n: int, seed: int, magnitude: float = 1.0) -> np.ndarray:
+def build_rows(n: int, seed: int, magnitude: float = 1.0, all_unusual: bool = False) -> np.ndarray:
     """n packed rows whose group scales cover 100..142.
 
     Per row a pattern: 40 % all groups ordinary, 30 % one unusual group, 30 % every
-    group drawn from 100..142.  Group values are N(0, magnitude) written with the
-    group's own scale byte s (x / 2^(s-127) rounded to e4m3 and saturated), so the
+    group drawn from 100..142 (all_unusual: every group of every row unusual).  Group
+    values are N(0, magnitude) written with the group's own scale byte s (x / 2^(s-127) rounded to e4m3 and saturated), so the
     dequantised magnitudes stay O(magnitude) whatever s is; for the smallest scales
     the codes saturate and the values are tiny."""
     rng = np.random.default_rng(seed)
@@ -50,6 +50,8 @@ def build_rows(n: int, seed: int, magnitude: float = 1.0) -> np.ndarray:
             s[rng.integers(W.N_GROUPS)] = rng.choice(UNUSUAL)
         elif kind >= 0.7:
             s = rng.integers(100, 143, size=W.N_GROUPS)
+        if all_unusual:
+            s = rng.choice(UNUSUAL, size=W.N_GROUPS)
         x = rng.standard_normal(W.NOPE) * magnitude
         scale = np.ldexp(1.0, s.astype(np.int64) - 127)
         codes = _e4m3_codes(x / np.repeat(scale, W.GROUP))
@@ -91,9 +93,7 @@ def test_every_group_of_a_row_unusual_at_once():
     """All rows in the index list have only unusual scale bytes (every converting
     lane takes the checked path), including the smallest groups that vanish in f16."""
     rng = np.random.default_rng(5)
-    rows = build_rows(256, seed=6)
-    for r in range(rows.shape[0]):
-        rows[r, W.SCALE_OFF:W.SCALE_OFF + W.N_GROUPS] = rng.choice(UNUSUAL, size=W.N_GROUPS)
+    rows = build_rows(256, seed=6, all_unusual=True)
     kv = torch.as_tensor(rows, device="cuda")
     idx = rng.permutation(256)[None, :200].astype(np.int32)
     q = torch.randn((1, 64, 512), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
