@@ -215,6 +215,21 @@ int sparse_mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t
                               void* out, float* lse, const smla_params* p, int32_t num_splits,
                               smla_stream_t stream);
 
+/*
+ * Test hook for the failure path of the decode kernels; the pages have no
+ * counterpart.  With block >= 0, every later launch of the decode kernels (any
+ * device, any thread) runs with one converter warp of every CTA withholding its
+ * "block filled" signal for block `block` (64 index slots) of its split, and with
+ * its bounded waits shortened to about 10 ms of SM clocks: the tensor-core warp's
+ * wait for that block then runs out, the CTA records SMLA_ERR_TIMEOUT in the device
+ * status word (smla_device_status), every role leaves through its bounded waits and
+ * the epilogue, and the launch completes without a fault; its outputs are undefined.
+ * CTAs whose split has no such block are unaffected.  block = -1 switches the hook
+ * off.  Returns SMLA_OK, or SMLA_ERR_INVALID_ARG for block < -1.  Not for use in
+ * production; calls made while it is on are not thread-safe with respect to it.
+ */
+int smla_test_inject_fault(int32_t block);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* smla_status_string(int status);
 

@@ -33,6 +33,7 @@ EXPORTED = (
     "sparse_mla_decode_paged",
     "smla_status_string",
     "smla_device_status",
+    "smla_test_inject_fault",
 )
 
 
@@ -74,6 +75,7 @@ def load() -> ctypes.CDLL:
     lib.smla_status_string.argtypes = [ctypes.c_int]
     lib.smla_status_string.restype = ctypes.c_char_p
     lib.smla_device_status.argtypes = [ctypes.POINTER(i32), i32]
+    lib.smla_test_inject_fault.argtypes = [i32]
     for name in EXPORTED:
         if name != "smla_status_string":
             getattr(lib, name).restype = ctypes.c_int

@@ -333,6 +333,12 @@ const char* smla_status_string(int status) {
   }
 }
 
+int smla_test_inject_fault(int32_t block) {
+  if (block < -1) return SMLA_ERR_INVALID_ARG;
+  smla::set_fault_block(block);
+  return SMLA_OK;
+}
+
 int smla_device_status(int32_t* status, int32_t clear) {
   if (status == nullptr) return SMLA_ERR_INVALID_ARG;
   int sms = 0;

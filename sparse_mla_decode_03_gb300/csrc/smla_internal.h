@@ -75,6 +75,10 @@ int check_device();
 int launch_step(const void* q, const void* kv_cache, const int32_t* indices, void* out,
                 float* lse, const smla_params* p, int S, void* workspace, cudaStream_t stream);
 
+// Test hook of smla_test_inject_fault: block index at which one converter warp of
+// every CTA of later decode launches withholds its "block filled" arrival (-1: off).
+void set_fault_block(int block);
+
 // Device address of the status word (kernels in other translation units record
 // their errors through it; device variables are not shared across them).
 cudaError_t status_word_address(int** ptr);
