@@ -61,33 +61,54 @@ int max_splits(const smla_params* p) {
   return granules < kMaxSplits ? granules : kMaxSplits;
 }
 
-// Plan: 1 CTA per SM is resident (the kernel uses ~210 KB of shared memory), so
-// choose S to minimise the modelled time below, preferring fewer splits on ties.
-int plan_splits(const smla_params* p, int sms) {
+// Step time model, in units of one 64-slot block of a CTA (one CTA per SM is
+// resident): waves * (blocks of the largest split + kFixedBlocks) + kCombineBlocks
+// when a second kernel merges the splits.  A wave holds `per_wave` CTAs: the SM
+// count for plain launches, (clusters the device holds at once) * S for clustered
+// ones, which can be fewer since a cluster's CTAs share one GPC.  The constants are
+// GB300 measurements: the prologue (first gathers, q) and epilogue (partials, merge)
+// of a CTA cost ~2.6 blocks, the combine launch ~0.5 block.
+constexpr double kFixedBlocks = 2.6;
+constexpr double kCombineBlocks = 0.5;
+
+double step_cost(const smla_params* p, int s, int64_t per_wave, bool fused) {
   const int groups = p->num_heads > 64 ? p->num_heads / 64 : 1;
-  const int64_t ctas_per_split = static_cast<int64_t>(p->batch) * groups;
-  const int smax = max_splits(p);
+  const int64_t ctas = static_cast<int64_t>(p->batch) * groups * s;
+  const int granules = (p->topk + 15) / 16;
+  const int gmax = (granules + s - 1) / s;                // granules of the largest split
+  const int blocks = (gmax * 16 + 63) / 64;
+  const int64_t waves = (ctas + per_wave - 1) / std::max<int64_t>(per_wave, 1);
+  return static_cast<double>(waves) * (blocks + kFixedBlocks) + (fused ? 0.0 : kCombineBlocks);
+}
+
+// Cost of S splits in the cheaper of the two launch forms; *fused tells which.
+int mode_cost(const smla_params* p, int s, int sms, double* cost, bool* fused) {
+  int clusters = 0;
+  if (smla::fused_clusters(p->num_heads, s, &clusters) != cudaSuccess) return SMLA_ERR_CUDA;
+  const double plain = step_cost(p, s, sms, false);
+  const double clustered = clusters > 0 ? step_cost(p, s, static_cast<int64_t>(clusters) * s, true)
+                                        : 1e300;
+  *fused = clustered <= plain;
+  *cost = std::min(plain, clustered);
+  return SMLA_OK;
+}
+
+// Plan: the split count of least modelled time, preferring fewer splits on ties.
+int plan_splits(const smla_params* p, int sms, int* S) {
   int best = 1;
   double best_cost = 1e300;
-  for (int s = 1; s <= smax; ++s) {
-    const int granules = (p->topk + 15) / 16;
-    const int gmax = (granules + s - 1) / s;              // granules of the largest split
-    const int tiles = (gmax * 16 + 127) / 128;
-    const int64_t waves = (ctas_per_split * s + sms - 1) / sms;
-    // In units of one steady-state 128-slot tile: the tiles of the largest split, the
-    // fixed prologue and epilogue, and the gather of the first tile's rows, which a
-    // CTA waits for in full before its first tile starts (measured: a full first tile
-    // costs ~0.8 tile more than a nearly empty one).  Beyond the cluster size the
-    // splits are merged by a second kernel.
-    const int first_rows = std::min(gmax * 16, 128);
-    const double cost = static_cast<double>(waves) * (tiles + 0.35 + 0.8 * first_rows / 128.0) +
-                        (s > 8 ? 0.6 : 0.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
+  for (int s = 1; s <= max_splits(p); ++s) {
+    double c = 0;
+    bool f = false;
+    const int st = mode_cost(p, s, sms, &c, &f);
+    if (st != SMLA_OK) return st;
+    if (c < best_cost - 1e-9) {
+      best_cost = c;
       best = s;
     }
   }
-  return best;
+  *S = best;
+  return SMLA_OK;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -104,15 +125,28 @@ int check_device() {
 // One whole decode step on validated arguments: one launch when the splits of a
 // query fit in a thread-block cluster (they merge their partials in the workspace
 // inside that launch), split + combine kernels otherwise.
+int plan_mode(const smla_params* p, int S, bool* fused) {
+  int sms = 0;
+  int st = current_device_sms(&sms);
+  if (st != SMLA_OK) return st;
+  double c = 0;
+  return mode_cost(p, S, sms, &c, fused);
+}
+
 int launch_step(const void* q, const void* kv_cache, const int32_t* indices, void* out,
                 float* lse, const smla_params* p, int S, void* workspace, cudaStream_t s) {
   const size_t bhs = static_cast<size_t>(p->batch) * p->num_heads * S;
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                              round256(bhs * kNope * sizeof(float)));
-  cudaError_t e = launch_decode_fused(q, kv_cache, indices, o_part, lse_part, out, lse,
-                                      p->batch, p->num_heads, p->topk, S, p->num_rows,
-                                      p->kv_row_stride, p->softmax_scale, s);
+  bool fused = false;
+  const int st = plan_mode(p, S, &fused);
+  if (st != SMLA_OK) return st;
+  cudaError_t e = cudaErrorNotSupported;
+  if (fused)
+    e = launch_decode_fused(q, kv_cache, indices, o_part, lse_part, out, lse, p->batch,
+                            p->num_heads, p->topk, S, p->num_rows, p->kv_row_stride,
+                            p->softmax_scale, s);
   if (e == cudaSuccess) return SMLA_OK;
   if (e != cudaErrorNotSupported) return SMLA_ERR_CUDA;
   e = launch_split(q, kv_cache, indices, o_part, lse_part, p->batch, p->num_heads, p->topk, S,
@@ -144,8 +178,7 @@ int resolve_splits(const smla_params* p, int32_t requested, int* S) {
   int sms = 0;
   const int st = current_device_sms(&sms);
   if (st != SMLA_OK) return st;
-  *S = plan_splits(p, sms);
-  return SMLA_OK;
+  return plan_splits(p, sms, S);
 }
 
 int check_tensors(const void* q, const void* kv, const int32_t* idx) {
@@ -176,10 +209,11 @@ int smla_decode_plan(const smla_params* p, int32_t num_splits, int32_t* splits, 
   int S = 0;
   st = resolve_splits(p, num_splits, &S);
   if (st != SMLA_OK) return st;
-  bool ok = false;
-  if (smla::fused_supported(p->num_heads, S, &ok) != cudaSuccess) return SMLA_ERR_CUDA;
+  bool f = false;
+  st = smla::plan_mode(p, S, &f);
+  if (st != SMLA_OK) return st;
   *splits = S;
-  *fused = ok ? 1 : 0;
+  *fused = f ? 1 : 0;
   return SMLA_OK;
 }
 

@@ -87,15 +87,19 @@ constexpr int kRegsConv = 88;
 constexpr int kRegsMma = 40;
 static_assert(kRegsSoft * 128 + kRegsConv * kConv + kRegsMma * 128 <= kLaunchRegs * kThreads,
               "register split exceeds the launch allocation");
-constexpr long long kWaitLimit = 2000000000LL;  // ~1 s of SM clocks
-constexpr long long kFaultWaitLimit = 20000000LL;  // ~10 ms, with the test hook on
+// Bounded waits, in units of 1024 SM clocks: ~1 s, and ~10 ms with the test hook on.
+constexpr uint32_t kWaitLimitK = 2000000u;
+constexpr uint32_t kFaultWaitLimitK = 20000u;
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kLazyMax = 8.0f;                // log2 headroom before the max is raised
+// log2 headroom before the running max is raised: P = 2^(s - m) <= 2^15 stays inside
+// the f16 range (65504) with its full 11-bit precision, and a rescale (which waits for
+// the previous value product) happens only when a score passes the max by 2^15
+constexpr float kLazyMax = 15.0f;
 constexpr int kMaxCluster = 8;                  // splits merged on chip (portable cluster size)
 enum : int { kSplitOnly = 0, kMergeL2 = 1 };
 
 // Named barriers (id 0 is __syncthreads).
-enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3 };
+enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 = 5 };
 
 // mbarriers.  FULL0/1: block buffer filled (one arrival per converter warp);
 // EMPTY0/1: value product of the block in that buffer done (buffer and P free);
@@ -116,11 +120,11 @@ struct Cfg {
   static constexpr int kPRow = 2 * NH;                     // bytes of one P row (token)
   static constexpr int kPBytes = kBlk * kPRow;
   static constexpr int kXOff = kPOff + ((kPBytes + 1023) / 1024) * 1024;
-  static constexpr int kXBytes = kBlk * NH * 4;            // score halves traded
+  // score halves traded; also the block-max transpose (NH heads x 65 floats)
+  static constexpr int kXBytes = NH * 65 * 4;
   static constexpr int kOnesOff = kXOff + ((kXBytes + 1023) / 1024) * 1024;  // 2 KB
   static constexpr int kMOff = kOnesOff + 2048;            // float [2][NH] running max (log2)
-  static constexpr int kRedOff = kMOff + 2 * NH * 4;       // float [2][NH]
-  static constexpr int kLOff = kRedOff + 2 * NH * 4;       // float [NH] denominators
+  static constexpr int kLOff = kMOff + 2 * NH * 4;         // float [NH] denominators
   static constexpr int kRinvOff = kLOff + NH * 4;          // float [NH] 1 / denominators
   static constexpr int kBarOff = kRinvOff + NH * 4;        // uint64 [B_COUNT]
   static constexpr int kTaddrOff = kBarOff + 8 * B_COUNT;  // uint32
@@ -300,8 +304,10 @@ __device__ __forceinline__ uint4 dq8_fast(uint32_t x, uint32_t y, uint32_t m) {
 }
 // 8 e4m3 bytes with scale byte s -> 8 f16, any s: the product is formed in fp32 and
 // rounded to f16 (subnormal results are rounded, not flushed); values beyond the f16
-// range become inf and are reported (SMLA_ERR_RANGE).
-__device__ __forceinline__ uint4 dequant8_f16(uint32_t x, uint32_t y, uint32_t s) {
+// range become inf and are reported (SMLA_ERR_RANGE).  Out of line: it serves only
+// rows with unusual scale bytes, and keeping it out of the converters' loop keeps
+// that loop small in the instruction cache.
+__device__ __noinline__ uint4 dequant8_checked(uint32_t x, uint32_t y, uint32_t s) {
   const float sc = ue8m0_to_f32(s);
   const uint32_t in[4] = {x & 0xffffu, x >> 16, y & 0xffffu, y >> 16};
   uint32_t o[4];
@@ -326,12 +332,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 
 // Bounded mbarrier wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_f,
-                                              long long limit) {
+                                              uint32_t limit_k) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
+    __nanosleep(32);   // a waiting warp leaves the issue slots to the warps at work
     if (*abort_f) return false;
-    if (clock64() - t0 > limit) {
+    if (clock64() - t0 > (static_cast<long long>(limit_k) << 10)) {
       *abort_f = 1;
       record_status(SMLA_ERR_TIMEOUT);
       return false;
@@ -343,7 +350,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // mbarrier (bounded), the others sleep on the named barrier, and every thread gets
 // the same verdict.
 __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volatile int* abort_f,
-                                           long long limit, bool poller, int id, int count) {
+                                           uint32_t limit, bool poller, int id, int count) {
   bool ok = true;
   if (poller) ok = wait_or_abort(bar, parity, abort_f, limit);
   __syncwarp();
@@ -351,7 +358,7 @@ __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volati
 }
 // Wait of one warp: lane 0 polls, the warp shares its verdict.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_f,
-                                          long long limit) {
+                                          uint32_t limit) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_f, limit);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -386,38 +393,19 @@ __device__ __forceinline__ bool idx_ok(int idx, int64_t num_rows, bool report) {
 }
 
 // ---------------------------------------------------------------------------
-// Row loading.  A row starting at byte address a (8-byte aligned) is read as 16-byte
-// chunks from a & ~15; sh = (a >> 3) & 1 is its shift in that grid.  8 lanes share a
-// row, lane q reading chunks q + 8j into register slot j (j = 0..4; 37 chunks, the
-// last read as 8 bytes when sh = 0, so nothing past the row is touched; with sh = 1
-// the first chunk starts 8 bytes before the row, inside the allocation because the
-// cache base is 16-byte aligned).  Chunk c holds row words 2c - sh and 2c + 1 - sh (a
-// word = 8 bytes).  Word w < 56: nope columns 8w..8w+7 (scale group w / 8); w = 56:
-// the 7 scales and the pad; w = 57..72: rope.
-//
-// Lane layout within a warp (4 rows): lane = qq + 4*rowbit + 8*qhi + 16*pairsel,
-// q = qq + 4*qhi, row = 2*pairsel + rowbit.  A 16-byte shared store is served in four
-// phases of 8 consecutive lanes; each phase holds 4 lanes of an even row and 4 lanes
-// of the odd row after it.  Every lane stores its chunk's even word (2c) in one
-// instruction and its odd word (2c + 1 or 2c - 1) in another: even words land on even
-// 16-byte units of their 128-byte row and odd words on odd ones, and the XOR swizzle
-// with row & 7 maps the even row and the odd row of a phase onto units of opposite
-// parity, so every store instruction is free of bank conflicts.
+// Row loading.  A row is 73 words of 8 bytes (rows are 8-byte aligned): word w < 56
+// holds nope columns 8w..8w+7 (scale group w / 8), word 56 the 7 scales and the pad,
+// words 57..72 the rope.  8 lanes share a row (lane = 8 * row + q); lane q reads words
+// q + 8k into register slot k (k = 0..8, and k = 9 for word 72 on lane 0), so slot
+// k < 7 of every lane is a nope word of group k, slot 7 is the scale word (lane 0) or
+// rope word 56 + q, slot 8 rope word 64 + q.  A 16-byte shared store of slot k by a
+// warp is served in four phases of 8 consecutive lanes, i.e. one row each, whose 8
+// words fill the 8 distinct 16-byte units of their 128-byte row: no bank conflicts.
 // ---------------------------------------------------------------------------
-constexpr int kSlots = 5;
+constexpr int kSlots = 10;
 
-template <int J>
-__device__ __forceinline__ uint4 load_slot(const uint8_t* base, int q, bool s) {
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  if (base == nullptr) return z;
-  const int c = q + 8 * J;
-  if (J < 4 || c < 36) return ldg_nc_u4(base + 16 * c);
-  if (c == 36) {
-    if (s) return ldg_nc_u4(base + 16 * c);
-    const uint2 v = ldg_nc_u2(base + 16 * c);
-    return make_uint4(v.x, v.y, 0u, 0u);
-  }
-  return z;
+__device__ __forceinline__ uint2 load_word(const uint8_t* row, int w) {
+  return row == nullptr ? make_uint2(0u, 0u) : ldg_nc_u2(row + 8 * w);
 }
 
 // prmt selecting byte g of the pair (a, b) into bits 8..15 of both halves, with byte
@@ -465,10 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Split sp = split_range(topk, S, s);
   const int nb = sp.nblocks;
   const int32_t* idx_row = indices + static_cast<int64_t>(b) * topk;
-  const long long limit = fault_block >= 0 ? kFaultWaitLimit : kWaitLimit;
+  const uint32_t limit = fault_block >= 0 ? kFaultWaitLimitK : kWaitLimitK;
 
   float* mbuf = reinterpret_cast<float*>(smem + C::kMOff);
-  float* red = reinterpret_cast<float*>(smem + C::kRedOff);
   float* lfin = reinterpret_cast<float*>(smem + C::kLOff);
   float* rinv = reinterpret_cast<float*>(smem + C::kRinvOff);
   const uint32_t bars = sbase + C::kBarOff;
@@ -477,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
   if (tid == 0) {
-    mbar_init(bar(B_FULL0), kConvWarps);
-    mbar_init(bar(B_FULL1), kConvWarps);
+    mbar_init(bar(B_FULL0), kConvWarps / 2);   // one set of converter warps per buffer
+    mbar_init(bar(B_FULL1), kConvWarps / 2);
     for (int i = B_EMPTY0; i <= B_SFULL1; ++i) mbar_init(bar(i), 1);
     mbar_init(bar(B_SEMPTY0), kSoftWarps);
     mbar_init(bar(B_SEMPTY1), kSoftWarps);
@@ -552,8 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait(B_QREADY, 0);
       auto qk = [&](int i) {
         const int u = i & 1;
-        if (!wait(B_FULL0 + u, (i >> 1) & 1)) return false;
-        if (i >= 2 && !wait(B_SEMPTY0 + u, ((i >> 1) - 1) & 1)) return false;
         const uint32_t aK = lK + static_cast<uint32_t>((u * kBuf) >> 4);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -569,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto pv = [&](int i) {
         const int u = i & 1;
-        if (!wait(B_PFULL, i & 1)) return false;
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int mb = 0; mb < 4; ++mb) {
@@ -592,22 +576,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         opaque();
         return true;
       };
-      // QK(p), QK(p+1), PV(p), PV(p+1): the softmax of block p overlaps QK(p+1)
+      // Issue order decided by readiness: the scores of block nq (its buffer filled,
+      // its scores buffer read by the softmax of block nq - 2; at most one block ahead
+      // of the value products) or the value product of block np (its P written).  Each
+      // barrier is tested without blocking, so a late converter set or a late softmax
+      // holds up only its own block.
+      int nq = 0, np = 0;
+      long long t_idle = clock64();
 #pragma unroll 1
-      for (int p = 0; ok && p < nb; p += 2) {
-        const int pe = min(p + 2, nb);
-#pragma unroll 1
-        for (int i = p; ok && i < pe; ++i) ok = qk(i);
-#pragma unroll 1
-        for (int i = p; ok && i < pe; ++i) ok = pv(i);
+      while (ok && np < nb) {
+        if (nq < nb && nq <= np + 1 && mbar_try_wait(bar(B_FULL0 + (nq & 1)), (nq >> 1) & 1) &&
+            (nq < 2 || mbar_try_wait(bar(B_SEMPTY0 + (nq & 1)), ((nq >> 1) - 1) & 1))) {
+          tc_fence_after();
+          opaque();
+          ok = qk(nq);
+          ++nq;
+          t_idle = clock64();
+        } else if (np < nq && mbar_try_wait(bar(B_PFULL), np & 1)) {
+          tc_fence_after();
+          opaque();
+          ok = pv(np);
+          ++np;
+          t_idle = clock64();
+        } else if (*abort_f) {
+          ok = false;
+        } else if (clock64() - t_idle <= (static_cast<long long>(limit) << 10)) {
+          __nanosleep(20);   // nothing ready: yield the issue slots to the warps at work
+        } else {
+          *abort_f = 1;
+          record_status(SMLA_ERR_TIMEOUT);
+          ok = false;
+        }
       }
       mma_commit(bar(B_ODONE));
       // Let the tensor pipe drain before the final barrier (tensor memory is freed
       // after it), also when another role left early.
-      if (!ok) mbar_wait(bar(B_ODONE), 0, kWaitLimit);
+      if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
     }
     // the bulk copy of q has landed before the CTA can leave
-    if (warp == kMmaWarp && lane == 0 && nb > 0) mbar_wait(bar(B_QRAW), 0, limit);
+    if (warp == kMmaWarp && lane == 0 && nb > 0)
+      mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
     // the cluster barrier of the merging epilogue, in step with the other roles
     if constexpr (MODE == kMergeL2) cluster_sync();
@@ -626,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xsw = static_cast<uint32_t>(t & (NH / 4 < 8 ? NH / 4 - 1 : 7));
     bool ok = nb > 0;
     int cur = 0;
+    bool have_m = false;   // the running max is set (a valid token has been seen)
     if (ok) {
       // ---- q: bf16 rows staged in buffer 1 -> stacked f16 Q operand; constant block
       ok = group_wait(bar(B_QRAW), 0, abort_f, limit, poller, kBarSoft, 128);
@@ -656,68 +665,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_QREADY));
       }
     }
+    // Each warp waits for its scores and for the P buffer on its own; warps w and w ^ 2
+    // (the two halves of the same tokens) meet at a 64-thread barrier to trade their
+    // halves, and all four meet once per block for the lazy-max vote.  Every warp
+    // executes the same sequence of named barriers whatever its verdicts, and a failed
+    // wait makes the vote fire, where the verdict is made uniform and the loop left.
+    const int pair_bar = kBarPair0 + (warp & 1);
     int vraw = ok ? raw_idx(idx_row, sp.t_begin + t, sp.t_end) : -1;
     for (int i = 0; ok && i < nb; ++i) {
       const int u = i & 1;
       const bool valid = idx_ok(vraw, num_rows, false);
       vraw = i + 1 < nb ? raw_idx(idx_row, sp.t_begin + (i + 1) * kBlk + t, sp.t_end) : -1;
-      if (!(ok = group_wait(bar(B_SFULL0 + u), (i >> 1) & 1, abort_f, limit, poller, kBarSoft,
-                            128)))
-        break;
-      tc_fence_after();
+      bool wok = warp_wait(bar(B_SFULL0 + u), (i >> 1) & 1, abort_f, limit);
       const uint32_t scols = tS + lane_base + u * 2 * NH + scol;
       float sv[HH];
-      {   // the half handed over first, then the half kept
-        float x[HH];
-        tmem_ld_n<HH>(scols + send0, x);
-        tmem_wait_ld();
+      if (wok) {
+        tc_fence_after();
+        // the half handed over first (8 columns at a time), then the half kept
 #pragma unroll
-        for (int k = 0; k < HH / 4; ++k)
-          st_shared_v4(xrow + ((static_cast<uint32_t>(send0 / 4 + k) ^ xsw) << 4),
-                       make_uint4(__float_as_uint(x[4 * k]), __float_as_uint(x[4 * k + 1]),
-                                  __float_as_uint(x[4 * k + 2]), __float_as_uint(x[4 * k + 3])));
+        for (int c8 = 0; c8 < HH; c8 += 8) {
+          float x[8];
+          tmem_ld<8>(scols + send0 + c8, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            st_shared_v4(xrow + ((static_cast<uint32_t>((send0 + c8) / 4 + k) ^ xsw) << 4),
+                         make_uint4(__float_as_uint(x[4 * k]), __float_as_uint(x[4 * k + 1]),
+                                    __float_as_uint(x[4 * k + 2]), __float_as_uint(x[4 * k + 3])));
+        }
+        tmem_ld_n<HH>(scols + keep0, sv);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SEMPTY0 + u));   // scores buffer u may be rewritten
       }
-      tmem_ld_n<HH>(scols + keep0, sv);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY0 + u));   // scores buffer u may be rewritten
-      bar_sync(kBarSoft, 128);                          // every half is in X
+      wok = bar_and(pair_bar, 64, wok);                   // both halves of the tokens are in X
+      // t = score * scale (log2 units) - running max (0 until the first valid token
+      // sets the max: every head gets its first finite max at that same block);
+      // masked tokens -inf
       float ex = -INFINITY;
-      {
+      if (wok) {
         const float* m_old = mbuf + cur * NH + keep0;
 #pragma unroll
         for (int k = 0; k < HH / 4; ++k) {
           const uint4 v = ld_shared_v4(xrow + ((static_cast<uint32_t>(keep0 / 4 + k) ^ xsw) << 4));
-          sv[4 * k] += __uint_as_float(v.x);
-          sv[4 * k + 1] += __uint_as_float(v.y);
-          sv[4 * k + 2] += __uint_as_float(v.z);
-          sv[4 * k + 3] += __uint_as_float(v.w);
+          float4 m4 = *reinterpret_cast<const float4*>(m_old + 4 * k);
+          if (!have_m) m4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          sv[4 * k] = fmaf(sv[4 * k] + __uint_as_float(v.x), scale_log2, -m4.x);
+          sv[4 * k + 1] = fmaf(sv[4 * k + 1] + __uint_as_float(v.y), scale_log2, -m4.y);
+          sv[4 * k + 2] = fmaf(sv[4 * k + 2] + __uint_as_float(v.z), scale_log2, -m4.z);
+          sv[4 * k + 3] = fmaf(sv[4 * k + 3] + __uint_as_float(v.w), scale_log2, -m4.w);
         }
+        if (valid) {
+          float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          sv[h] = valid ? sv[h] * scale_log2 : -INFINITY;
-          ex = fmaxf(ex, sv[h] - m_old[h]);   // NaN (-inf - -inf) is ignored by fmaxf
+          for (int h = 0; h < HH; ++h) e4[h & 3] = fmaxf(e4[h & 3], sv[h]);
+          ex = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
+          if (!have_m) ex = INFINITY;   // the first valid token sets the running max
+        } else {
+#pragma unroll
+          for (int h = 0; h < HH; ++h) sv[h] = -INFINITY;
         }
-        if (!valid) ex = -INFINITY;
       }
       // One barrier in the common case: no score passed the running max by more than
       // the headroom.  (It also ends every thread's reads of X for this block.)
-      if (bar_or(kBarSoft, 128, ex > kLazyMax)) {
+      if (bar_or(kBarSoft, 128, !wok || ex > kLazyMax)) {
+        if (!(ok = bar_and(kBarSoft, 128, wok))) break;   // a wait ran out: leave together
         // Raise the running max to the exact block max; rescale O (and with it the
         // denominator row) by 2^(m_old - m_new).  Warps 0-1 hold heads [0, NH/2),
         // warps 2-3 heads [NH/2, NH), 32 tokens each.
-#pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          const float m = warp_max(sv[h]);
-          if (lane == (h & 31)) red[(warp & 1) * NH + keep0 + h] = m;
-        }
-        bar_sync(kBarSoft, 128);
         const float* m_old = mbuf + cur * NH;
         float* m_new = mbuf + (cur ^ 1) * NH;
-        if (tid < NH) m_new[tid] = fmaxf(m_old[tid], fmaxf(red[tid], red[NH + tid]));
+        // block max per head through X (free again: every thread has read its half),
+        // transposed with a skew of 65 floats per head so both the writes (one head,
+        // consecutive tokens) and the reads (consecutive heads) are conflict-free
+        float* xt = reinterpret_cast<float*>(smem + C::kXOff);
+#pragma unroll
+        for (int h = 0; h < HH; ++h)
+          xt[(keep0 + h) * 65 + t] = have_m ? sv[h] + m_old[keep0 + h] : sv[h];
         bar_sync(kBarSoft, 128);
-        if (i > 0) {
+        if (tid < NH) {
+          float m = -INFINITY;
+#pragma unroll 8
+          for (int tk = 0; tk < kBlk; ++tk) m = fmaxf(m, xt[tid * 65 + tk]);
+          m_new[tid] = fmaxf(m_old[tid], m);
+        }
+        bar_sync(kBarSoft, 128);
+        if (have_m) {
           // O holds the value products up to block i - 1: let the last one finish
           if (!(ok = group_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f,
                                 limit, poller, kBarSoft, 128)))
@@ -727,10 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hc = 0; hc < NH; hc += 8) {
             float f[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float mn = m_new[hc + k];
-              f[k] = (mn == -INFINITY) ? 1.f : exp2f(m_old[hc + k] - mn);
-            }
+            for (int k = 0; k < 8; ++k) f[k] = exp2f(m_old[hc + k] - m_new[hc + k]);
 #pragma unroll 1
             for (int mb = 0; mb < 4; ++mb) {
               float o[8];
@@ -743,22 +774,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        cur ^= 1;
-      }
-      {
-        const float* m = mbuf + cur * NH + keep0;
+        // re-base t on the new max
 #pragma unroll
         for (int h = 0; h < HH; ++h)
-          // sv = -inf (masked) gives 0; m = -inf only while every score so far is
-          // masked, and then sv is -inf too
-          sv[h] = (sv[h] == -INFINITY) ? 0.f : fast_exp2(sv[h] - m[h]);
+          sv[h] = sv[h] + ((have_m ? m_old[keep0 + h] : 0.f) - m_new[keep0 + h]);
+        have_m = true;
+        cur ^= 1;
       }
-      // P is single-buffered: the value product of block i - 1 must have read it
-      if (i > 0 && !(ok = group_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f,
-                                     limit, poller, kBarSoft, 128)))
-        break;
-      {   // row t of P (token-major, heads contiguous): this thread's heads
-        const uint32_t prow = sbase + C::kPOff;
+#pragma unroll
+      for (int h = 0; h < HH; ++h) sv[h] = fast_exp2(sv[h]);   // 2^-inf = 0 (masked)
+      // P is single-buffered: the value product of block i - 1 must have read it.  A
+      // warp whose wait runs out skips its part of P; the abort flag it set makes the
+      // next block's vote fire (or the MMA warp give up on this block's P).
+      if (i == 0 || warp_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f, limit)) {
+        const uint32_t prow = sbase + C::kPOff;   // row t: token-major, heads contiguous
 #pragma unroll
         for (int k = 0; k < HH / 8; ++k) {
           uint4 v;
@@ -768,11 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.w = pack_f16x2(sv[8 * k + 6], sv[8 * k + 7]);
           st_shared_v4(prow + swz_offset(t, keep0 / 8 + k, C::kPRow), v);
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL));
     }
     // the final running max into mbuf[0, NH) for the epilogue
     bar_sync(kBarSoft, 128);
@@ -782,111 +811,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConv) : "memory");
     // ===================== converters =====================
+    // Two sets of 8 warps: set 0 fills buffer 0 with the even blocks, set 1 buffer 1
+    // with the odd blocks.  A warp converts 8 rows of its block (two quads of 4 rows,
+    // 8 lanes per row) from registers, then loads the same rows of its next block
+    // (two blocks on), so each warp has only one block of loads in flight.
     const int cw = warp - kConvWarp0;            // 0..15
     const int wt = tid - kConvWarp0 * 32;        // 0..511
-    const int q8 = (lane & 3) + 4 * ((lane >> 3) & 1);   // chunk lane within the row
-    const int rb = 4 * cw + 2 * (lane >> 4) + ((lane >> 2) & 1);   // row of the block
-    const int scale_src = (lane & 0x14) | 8;     // lane with q8 = 4 of the same row
-    const bool lane_q0 = q8 == 0;
-    const uint32_t rx = static_cast<uint32_t>(rb & 7);
-    uint4 c[2][kSlots];
-    bool sh[2] = {false, false};
-    int nraw = -1;                               // stored index of this lane's row, 2 blocks ahead
-    bool ok = nb > 0;
-    auto row_base = [&](int raw, bool report, bool* shift) {
-      const uint8_t* row =
-          idx_ok(raw, num_rows, report) ? kv + static_cast<int64_t>(raw) * stride : nullptr;
-      *shift = ((reinterpret_cast<uintptr_t>(row) >> 3) & 1) != 0;
-      return reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(row) &
-                                              ~static_cast<uintptr_t>(15));
+    const int set = cw >> 3;
+    const int q8 = lane & 7;                     // word lane within the row
+    const int rb0 = 8 * (cw & 7) + (lane >> 3);  // row of quad 0 (quad 1: + 4)
+    const int row_lane0 = lane & ~7;             // lane q = 0 of this row (holds the scales)
+    uint2 c[2][kSlots];                          // [quad][slot]
+    int nraw[2] = {-1, -1};                      // stored indices of the rows, 2 blocks ahead
+    bool ok = set < nb;
+    auto row_of = [&](int raw, bool report) -> const uint8_t* {
+      return idx_ok(raw, num_rows, report) ? kv + static_cast<int64_t>(raw) * stride : nullptr;
+    };
+    auto load_rows = [&](int i) {   // rows of block i (nraw) into c; indices of block i + 2
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const uint8_t* row = row_of(i < nb ? nraw[g] : -1, q8 == 0);
+#pragma unroll
+        for (int k = 0; k < 9; ++k) c[g][k] = load_word(row, q8 + 8 * k);
+        c[g][9] = load_word(q8 == 0 ? row : nullptr, 72);
+        nraw[g] = raw_idx(idx_row, sp.t_begin + (i + 2) * kBlk + rb0 + 4 * g, sp.t_end);
+      }
     };
     if (ok) {
-      // ---- prologue: indices and the rows of blocks 0 and 1 ----
-      const int r0 = raw_idx(idx_row, sp.t_begin + rb, sp.t_end);
-      const int r1 = raw_idx(idx_row, sp.t_begin + kBlk + rb, sp.t_end);
-      nraw = raw_idx(idx_row, sp.t_begin + 2 * kBlk + rb, sp.t_end);
-      const uint8_t* b0 = row_base(r0, lane_q0, &sh[0]);
-      c[0][0] = load_slot<0>(b0, q8, sh[0]);
-      c[0][1] = load_slot<1>(b0, q8, sh[0]);
-      c[0][2] = load_slot<2>(b0, q8, sh[0]);
-      c[0][3] = load_slot<3>(b0, q8, sh[0]);
-      c[0][4] = load_slot<4>(b0, q8, sh[0]);
-      const uint8_t* b1 = row_base(r1, lane_q0, &sh[1]);
-      c[1][0] = load_slot<0>(b1, q8, sh[1]);
-      c[1][1] = load_slot<1>(b1, q8, sh[1]);
-      c[1][2] = load_slot<2>(b1, q8, sh[1]);
-      c[1][3] = load_slot<3>(b1, q8, sh[1]);
-      c[1][4] = load_slot<4>(b1, q8, sh[1]);
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        nraw[g] = raw_idx(idx_row, sp.t_begin + set * kBlk + rb0 + 4 * g, sp.t_end);
+      load_rows(set);
     }
-    auto convert = [&](auto uc, int i) {
-      constexpr int u = decltype(uc)::value;
-      // rows of block i + 2, read into this buffer's registers as they are freed
-      const bool has_n2 = i + 2 < nb;
-      bool nsh = false;
-      const uint8_t* nbase = row_base(has_n2 ? nraw : -1, lane_q0, &nsh);
-      nraw = raw_idx(idx_row, sp.t_begin + (i + 3) * kBlk + rb, sp.t_end);
-      // scale word of this lane's row (word 56: chunk 28, slot 3 of lane q8 = 4)
-      const bool shf = sh[u];
-      const uint32_t lo = __shfl_sync(0xffffffffu, shf ? c[u][3].z : c[u][3].x, scale_src);
-      const uint32_t hi = __shfl_sync(0xffffffffu, shf ? c[u][3].w : c[u][3].y, scale_src);
+    // Word q + 8k (k < 7) of row r lands in slab k & 3, row r + 64 (k >> 2), 16-byte
+    // unit q (XOR-swizzled with the row): this lane's base plus a compile-time offset.
+    const uint32_t rx0 = static_cast<uint32_t>(rb0 & 7);
+    // Converts quad g (runtime 0 or 1) of block i from d (its register slots).  One
+    // copy of this code serves both quads, and the checked path of unusual scale
+    // bytes is a call, so the converters' loop stays small in the instruction cache.
+    auto convert = [&](const uint2 (&d)[kSlots], int g, int i) {
+      const uint32_t rx = rx0 ^ (4u * g);
+      const uint32_t rowq = static_cast<uint32_t>(rb0 + 4 * g) * 128;
+      const uint32_t buf = sbase + (i & 1) * kBuf;
+      // scale word of this lane's row (word 56: slot 7 of lane q = 0)
+      const uint32_t lo = __shfl_sync(0xffffffffu, d[7].x, row_lane0);
+      const uint32_t hi = __shfl_sync(0xffffffffu, d[7].y, row_lane0);
       const bool masked = (lo | (hi & 0x00ffffffu)) == 0u;   // a zero-filled row
       const bool fast = __all_sync(0xffffffffu, masked || scales_fast(lo, hi));
       // f16 exponent field (s - 112) << 2 of each group's scale; byte 7 stays zero
       const uint32_t tlo = masked ? 0u : (lo - 0x70707070u) << 2;
       const uint32_t thi = masked ? 0u : ((hi & 0x00ffffffu) - 0x00707070u) << 2;
-      const uint32_t rowa = sbase + u * kBuf + rb * 128;
-      bool bad = false;
-      auto put = [&](int w, uint32_t x, uint32_t y) {
-        if (w >= 0 && w < 56) {
-          const int g = w >> 3;
-          const uint32_t addr = rowa + ((g & 3) << 14) + ((g & 4) << 11) +
-                                (((static_cast<uint32_t>(w) & 7u) ^ rx) << 4);
-          uint4 v;
-          if (fast) {
-            v = dq8_fast(x, y, prmt2(tlo, thi, 0x0707u | (g << 4) | (g << 12)));
-          } else {
-            const uint32_t sb = ((g < 4 ? lo : hi) >> (8 * (g & 3))) & 0xffu;
-            v = dequant8_f16(x, y, sb);
-          }
-          st_shared_v4(addr, v);
-        } else if (w >= 57 && w <= 72) {
-          const uint32_t k = static_cast<uint32_t>(w - 57);
-          const uint32_t addr = rowa + 3 * kSlab + 64 * 128 + ((((k >> 1) ^ rx)) << 4) +
-                                ((k & 1u) << 3);
-          const uint2 v = make_uint2(bf16x2_to_f16x2(x), bf16x2_to_f16x2(y));
-          bad |= f16x2_has_inf_or_nan(v.x) | f16x2_has_inf_or_nan(v.y);
-          st_shared_v2(addr, v);
+      const uint32_t an = buf + rowq + ((static_cast<uint32_t>(q8) ^ rx) << 4);
+      // FAST: every scale byte of the warp's rows in [113, 134] (exact f16x2 multiply);
+      // otherwise the checked fp32 path, out of line.  One branch per quad.
+      if (fast) {
+#pragma unroll
+        for (int k = 0; k < 7; ++k) {
+          // prmt: scale byte k of (tlo, thi) into bits 8..15 and 24..31, zero elsewhere
+          const uint32_t m = prmt2(tlo, thi, 0x0707u + 0x1010u * k);
+          st_shared_v4(an + (k & 3) * kSlab + (k >> 2) * 64 * 128, dq8_fast(d[k].x, d[k].y, m));
         }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 7; ++k) {
+          const uint32_t sb = ((k < 4 ? lo : hi) >> (8 * (k & 3))) & 0xffu;
+          st_shared_v4(an + (k & 3) * kSlab + (k >> 2) * 64 * 128, dequant8_checked(d[k].x, d[k].y, sb));
+        }
+      }
+      // rope: word 56 + q (slot 7, q >= 1), 64 + q (slot 8), 72 (slot 9, q = 0) is
+      // rope word r = w - 57: f16 8 bytes at unit r / 2, half r % 2 of the rope row
+      bool bad = false;
+      const uint32_t rope_base = buf + 3 * kSlab + 64 * 128 + rowq;
+      auto rope = [&](int r, uint2 v2) {
+        const uint2 v = make_uint2(bf16x2_to_f16x2(v2.x), bf16x2_to_f16x2(v2.y));
+        bad |= f16x2_has_inf_or_nan(v.x) | f16x2_has_inf_or_nan(v.y);
+        st_shared_v2(rope_base + (((static_cast<uint32_t>(r) >> 1) ^ rx) << 4) + (r & 1) * 8, v);
       };
-      auto chunk = [&](auto jc) {
-        constexpr int J = decltype(jc)::value;
-        const int ci = q8 + 8 * J;
-        const uint4 cj = c[u][J];
-        put(2 * ci, shf ? cj.z : cj.x, shf ? cj.w : cj.y);                       // even word
-        put(shf ? 2 * ci - 1 : 2 * ci + 1, shf ? cj.x : cj.z, shf ? cj.y : cj.w);  // odd word
-        c[u][J] = load_slot<J>(nbase, q8, nsh);
-      };
-      chunk(std::integral_constant<int, 0>{});
-      chunk(std::integral_constant<int, 1>{});
-      chunk(std::integral_constant<int, 2>{});
-      chunk(std::integral_constant<int, 3>{});
-      chunk(std::integral_constant<int, 4>{});
-      sh[u] = nsh;
+      if (q8 >= 1) rope(q8 - 1, d[7]);
+      rope(q8 + 7, d[8]);
+      if (q8 == 0) rope(15, d[9]);
       if (bad) record_status(SMLA_ERR_RANGE);
     };
-    for (int i = 0; ok && i < nb; ++i) {
+    for (int i = set; ok && i < nb; i += 2) {
       const int u = i & 1;
       // buffer u is free once the value product of block i - 2 is done; buffer 1
       // first holds the staged q rows until the softmax warps have converted them
       if (i >= 2) ok = warp_wait(bar(B_EMPTY0 + u), ((i >> 1) & 1) ^ 1, abort_f, limit);
       else if (i == 1) ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
       if (!ok) break;
-      if (u == 0) convert(std::integral_constant<int, 0>{}, i);
-      else convert(std::integral_constant<int, 1>{}, i);
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        uint2 d[kSlots];
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j) d[j] = g ? c[1][j] : c[0][j];
+        convert(d, g, i);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       // (the test hook withholds one warp's arrival, so the MMA warp's wait runs out)
-      if (lane == 0 && !(i == fault_block && cw == 0)) mbar_arrive(bar(B_FULL0 + u));
+      if (lane == 0 && !(i == fault_block && (cw & 7) == 0)) mbar_arrive(bar(B_FULL0 + u));
+      if (i + 2 < nb) load_rows(i + 2);
     }
 
     // ===================== epilogue =====================
@@ -1055,12 +1079,13 @@ cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices
                              g_fault_block.load(std::memory_order_relaxed));
 }
 
-// Whether a cluster of S split CTAs fits on the device: asked once per (device, S).
+// How many clusters of S split CTAs the device holds at once (0: such a cluster does
+// not fit, or S > 8): asked once per (device, S).
 template <int NH, int MODE>
-cudaError_t cluster_fits(int dev, int S, bool* fits) {
-  static signed char answer[kMaxDevices][kMaxCluster + 1] = {};   // 0 unknown, 1 yes, -1 no
+cudaError_t cluster_count(int dev, int S, int* clusters) {
+  static int answer[kMaxDevices][kMaxCluster + 1] = {};   // 0 unknown, else count + 1
   if (S < 1 || S > kMaxCluster) {
-    *fits = false;
+    *clusters = 0;
     return cudaSuccess;
   }
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -1082,10 +1107,18 @@ cudaError_t cluster_fits(int dev, int S, bool* fits) {
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, split_kernel<NH, MODE>, &cfg);
     if (e != cudaSuccess) return e;
-    answer[dev][S] = n > 0 ? 1 : -1;
+    answer[dev][S] = (n > 0 ? n : 0) + 1;
   }
-  *fits = answer[dev][S] > 0;
+  *clusters = answer[dev][S] - 1;
   return cudaSuccess;
+}
+
+template <int NH, int MODE>
+cudaError_t cluster_fits(int dev, int S, bool* fits) {
+  int n = 0;
+  const cudaError_t e = cluster_count<NH, MODE>(dev, S, &n);
+  *fits = n > 0;
+  return e;
 }
 
 template <int NH, int MODE>
@@ -1158,14 +1191,14 @@ cudaError_t launch_decode_fused(const void* q, const void* kv, const int32_t* in
   }
 }
 
-cudaError_t fused_supported(int H, int S, bool* supported) {
+cudaError_t fused_clusters(int H, int S, int* clusters) {
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   switch (H) {
-    case 16: return cluster_fits<16, kMergeL2>(dev, S, supported);
-    case 32: return cluster_fits<32, kMergeL2>(dev, S, supported);
-    default: return cluster_fits<64, kMergeL2>(dev, S, supported);
+    case 16: return cluster_count<16, kMergeL2>(dev, S, clusters);
+    case 32: return cluster_count<32, kMergeL2>(dev, S, clusters);
+    default: return cluster_count<64, kMergeL2>(dev, S, clusters);
   }
 }
 

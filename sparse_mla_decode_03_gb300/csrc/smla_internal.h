@@ -48,8 +48,9 @@ cudaError_t launch_decode_fused(const void* q, const void* kv, const int32_t* in
                                 int H, int topk, int S, int64_t num_rows, int64_t stride,
                                 float softmax_scale, cudaStream_t stream);
 
-// Whether launch_decode_fused can run S splits of H heads on the current device.
-cudaError_t fused_supported(int H, int S, bool* supported);
+// How many clusters of S splits of H heads the current device holds at once for
+// launch_decode_fused (0: it cannot run them).
+cudaError_t fused_clusters(int H, int S, int* clusters);
 
 // Launches the combine kernel over B * H (batch, head) pairs.
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int H, int S,
@@ -69,9 +70,14 @@ cudaError_t launch_paged_rows(const int32_t* indices, const int32_t* block_table
 // smla_status (SMLA_ERR_UNSUPPORTED_DEVICE or SMLA_ERR_CUDA).
 int check_device();
 
+// The launch form of a decode step with S splits on the current device: *fused is
+// true when the clustered launch (splits merged on chip) is modelled faster than
+// split + combine and fits.  Returns an smla_status.
+int plan_mode(const smla_params* p, int S, bool* fused);
+
 // One whole decode step (sparse_mla_decode after argument checks): S splits, the
-// split partials in `workspace` (laid out as smla_workspace_size describes).
-// Returns an smla_status.
+// split partials in `workspace` (laid out as smla_workspace_size describes), in the
+// form plan_mode chooses.  Returns an smla_status.
 int launch_step(const void* q, const void* kv_cache, const int32_t* indices, void* out,
                 float* lse, const smla_params* p, int S, void* workspace, cudaStream_t stream);
 
