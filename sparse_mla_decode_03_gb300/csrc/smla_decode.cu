@@ -103,38 +103,54 @@ enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 =
 
 // mbarriers.  FULL0/1: block buffer filled (one arrival per converter warp);
 // EMPTY0/1: value product of the block in that buffer done (buffer and P free);
-// SFULL0/1: scores in tensor-memory buffer 0/1; SEMPTY0/1: softmax has read them;
-// PFULL: P written; ODONE: all MMAs done; QRAW: the bf16 q rows copied into buffer 1;
-// QREADY: the stacked f16 Q and the constant block written.
+// SFULL0/1: scores in tensor-memory buffer 0/1 (one buffer, SFULL0, with Q in tensor
+// memory); SEMPTY0/1: softmax has read them; PFULL0/1: P buffer 0/1 written (one
+// buffer, PFULL0, with Q in shared memory); ODONE: all MMAs done; QRAW: the bf16 q
+// rows copied into buffer 1 (Q in shared memory); QREADY: the stacked f16 Q and the
+// constant block written.
 enum Bar : int {
   B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1,
-  B_PFULL, B_ODONE, B_QRAW, B_QREADY, B_COUNT
+  B_PFULL0, B_PFULL1, B_ODONE, B_QRAW, B_QREADY, B_COUNT
 };
 
 template <int NH>
 struct Cfg {
-  static constexpr int kHalf = NH / 2;                     // heads per softmax thread
+  // Q in tensor memory (the score MMA's A operand, scores transposed: heads as M) for
+  // 64 heads, where 2 NH = 128 stacked query rows fill the MMA's M; Q in shared
+  // memory (tokens as M) for fewer heads.
+  static constexpr bool kTS = NH == 64;
+  static constexpr int kHalf = NH / 2;                     // heads per softmax thread (SS)
   static constexpr int kQSlab = 2 * NH * 128;              // stacked Q: 2 NH rows x 128 B
   static constexpr int kQOff = 2 * kBuf;
-  static constexpr int kPOff = kQOff + 4 * kQSlab;
-  static constexpr int kPRow = 2 * NH;                     // bytes of one P row (token)
+  // P: SS [64 tokens][NH] (MN-major B operand), one buffer; TS [NH heads][64 tokens]
+  // (K-major B operand, 128-byte rows), two buffers
+  static constexpr int kPOff = kTS ? 2 * kBuf : kQOff + 4 * kQSlab;
+  static constexpr int kPRow = 2 * NH;                     // bytes of one P row (SS: token)
   static constexpr int kPBytes = kBlk * kPRow;
-  static constexpr int kXOff = kPOff + ((kPBytes + 1023) / 1024) * 1024;
-  // score halves traded; also the block-max transpose (NH heads x 65 floats)
-  static constexpr int kXBytes = NH * 65 * 4;
+  static constexpr int kPStride = ((kPBytes + 1023) / 1024) * 1024;
+  static constexpr int kPBufs = kTS ? 2 : 1;
+  static constexpr int kXOff = kPOff + kPBufs * kPStride;
+  // SS: score halves traded, and the block-max transpose (NH heads x 65 floats);
+  // TS: 32 partial scores per thread (128 rows of 128 bytes)
+  static constexpr int kXBytes = kTS ? 128 * 128 : NH * 65 * 4;
   static constexpr int kOnesOff = kXOff + ((kXBytes + 1023) / 1024) * 1024;  // 2 KB
   static constexpr int kMOff = kOnesOff + 2048;            // float [2][NH] running max (log2)
   static constexpr int kLOff = kMOff + 2 * NH * 4;         // float [NH] denominators
   static constexpr int kRinvOff = kLOff + NH * 4;          // float [NH] 1 / denominators
-  static constexpr int kBarOff = kRinvOff + NH * 4;        // uint64 [B_COUNT]
+  static constexpr int kMxOff = kRinvOff + NH * 4;         // float [128] block maxima (TS)
+  static constexpr int kAlphaOff = kMxOff + 128 * 4;       // float [NH] rescale factors (TS)
+  static constexpr int kBarOff = kAlphaOff + NH * 4;       // uint64 [B_COUNT]
   static constexpr int kTaddrOff = kBarOff + 8 * B_COUNT;  // uint32
   static constexpr int kAbortOff = kTaddrOff + 4;          // int
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
-  // S^T (two buffers of 2 NH columns) and O^T (4 x NH)
-  static constexpr uint32_t kTmemCols = 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
+  // TS: Q (128 columns), S^T (128), O^T (4 x NH); SS: S^T (two buffers of 2 NH
+  // columns) and O^T (4 x NH)
+  static constexpr uint32_t kTmemCols = kTS ? 512 : 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
+  static constexpr uint32_t kTQ = 0, kTS_S = kTS ? 128 : 0, kTO = kTS ? 256 : 4 * NH;
   static constexpr uint32_t kPSwz = NH == 64 ? SWZ_128B : NH == 32 ? SWZ_64B : SWZ_32B;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(NH * 64 <= kBuf / 2, "the staged q rows fit in a block buffer");
+  static_assert(kTS || NH * 64 <= kBuf / 2, "the staged q rows fit in a block buffer");
+  static_assert(!kTS || 4 * NH + 256 <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_smla_status, 0, code); }
@@ -469,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = B_EMPTY0; i <= B_SFULL1; ++i) mbar_init(bar(i), 1);
     mbar_init(bar(B_SEMPTY0), kSoftWarps);
     mbar_init(bar(B_SEMPTY1), kSoftWarps);
-    mbar_init(bar(B_PFULL), kSoftWarps);
+    mbar_init(bar(B_PFULL0), kSoftWarps);
+    mbar_init(bar(B_PFULL1), kSoftWarps);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_QRAW), 1);
     mbar_init(bar(B_QREADY), kSoftWarps);
@@ -489,16 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kernel in the stream may run until here.
   grid_dep_wait();
   grid_dep_launch();
-  const uint32_t tS = tmem;            // S^T buffer u: columns [2 NH u, 2 NH (u + 1))
-  const uint32_t tO = tmem + 4 * NH;   // O^T block mb: columns [4 NH + mb NH, ...)
+  // SS: S^T buffer u at columns [2 NH u, 2 NH (u + 1)), O^T block mb at 4 NH + mb NH;
+  // TS: Q at 0..127, S^T at 128..255, O^T block mb at 256 + mb NH
+  const uint32_t tQ = tmem + C::kTQ;
+  const uint32_t tS = tmem + C::kTS_S;
+  const uint32_t tO = tmem + C::kTO;
 
   if (warp >= kMmaWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma) : "memory");
     // ===================== MMA issuer =====================
     if (warp == kMmaWarp && lane == 0 && nb > 0) {
-      // The bf16 q rows h0..h0+NH-1 (contiguous, NH KB) into block buffer 1, where
+      // SS: the bf16 q rows h0..h0+NH-1 (contiguous, NH KB) into block buffer 1, where
       // the softmax warps convert them into the stacked Q operand.
-      {
+      if constexpr (!C::kTS) {
         const uint8_t* src =
             reinterpret_cast<const uint8_t*>(q + (static_cast<int64_t>(b) * H + h0) * kQkDim);
         mbar_arrive_expect_tx(bar(B_QRAW), NH * 1024);
@@ -506,8 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < NH / 16; ++k)
           bulk_g2s(sbase + kBuf + k * 16384, src + k * 16384, 16384, bar(B_QRAW));
       }
-      constexpr uint32_t kIdescQK = idesc_f16(128, 2 * NH, false, false);
-      constexpr uint32_t kIdescPV = idesc_f16(128, NH, true, true);
+      // SS: S^T (tokens x stacked heads) = stacked K . stacked Q^T, both from shared
+      // memory; TS: S (stacked heads x stacked tokens) = Q (tensor memory) . K^T.
+      // PV: O^T += V^T . P with V^T the MN-major view of the block; P is MN-major
+      // ([token][head]) in SS, K-major ([head][token]) in TS.
+      constexpr uint32_t kIdescQK = idesc_f16(128, C::kTS ? 128 : 2 * NH, false, false);
+      constexpr uint32_t kIdescPV = idesc_f16(128, NH, true, !C::kTS);
       // Descriptors as 32-bit halves: moving a start address by X bytes adds X >> 4 to
       // the low half (addresses stay below 256 KB, so the 14-bit field never
       // carries); the high halves (stride, swizzle) are fixed.
@@ -516,7 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // start field (bits 0-13) by the byte offset >> 4, the leading-offset field
       // (bits 16-29) by the change of the leading offset >> 4.
       const uint64_t dK = smem_desc(sbase, 16, 1024, SWZ_128B);
-      const uint64_t dP = smem_desc(sbase + C::kPOff, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
+      const uint64_t dP = C::kTS ? smem_desc(sbase + C::kPOff, 16, 1024, SWZ_128B)
+                                 : smem_desc(sbase + C::kPOff, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
       const uint32_t hi = static_cast<uint32_t>(dK >> 32);
       const uint32_t hiP = static_cast<uint32_t>(dP >> 32);
       uint32_t lK = static_cast<uint32_t>(dK), lP = static_cast<uint32_t>(dP);
@@ -543,12 +568,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f16_ss_hl(tS + u * 2 * NH, aK + static_cast<uint32_t>((j * kSlab + k * 32) >> 4),
-                          hi, lK + lo_of(C::kQOff + j * C::kQSlab + k * 32, 16), hi,
-                          kIdescQK, (j | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (C::kTS)   // K step 16: 8 columns of Q, 32 bytes of the slab
+              mma_f16_ts_hl(tS, tQ + static_cast<uint32_t>(8 * (4 * j + k)),
+                            aK + static_cast<uint32_t>((j * kSlab + k * 32) >> 4), hi,
+                            kIdescQK, (j | k) != 0 ? 1u : 0u);
+            else
+              mma_f16_ss_hl(tS + u * 2 * NH, aK + static_cast<uint32_t>((j * kSlab + k * 32) >> 4),
+                            hi, lK + lo_of(C::kQOff + j * C::kQSlab + k * 32, 16), hi,
+                            kIdescQK, (j | k) != 0 ? 1u : 0u);
+          }
         }
-        mma_commit(bar(B_SFULL0 + u));
+        mma_commit(bar(B_SFULL0 + (C::kTS ? 0 : u)));
         opaque();
         return true;
       };
@@ -567,9 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t st = u * kBuf + kV3 + ks * 2048;
               a = lK + lo_of(st, C::kOnesOff - st);
             }
-            mma_f16_ss_hl(tO + mb * NH, a, hi,
-                          lP + static_cast<uint32_t>((ks * 16 * C::kPRow) >> 4), hiP, kIdescPV,
-                          ks > 0 ? 1u : acc0);
+            // K step of 16 tokens: SS 16 P rows down, TS 32 bytes along each P row
+            const uint32_t bP = C::kTS ? static_cast<uint32_t>((u * C::kPStride + ks * 32) >> 4)
+                                       : static_cast<uint32_t>((ks * 16 * C::kPRow) >> 4);
+            mma_f16_ss_hl(tO + mb * NH, a, hi, lP + bP, hiP, kIdescPV, ks > 0 ? 1u : acc0);
           }
         }
         mma_commit(bar(B_EMPTY0 + u));
@@ -585,14 +617,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long t_idle = clock64();
 #pragma unroll 1
       while (ok && np < nb) {
+        // scores buffer free: SS two buffers (read by the softmax of block nq - 2), TS
+        // one (read by the softmax of block nq - 1)
+        const bool s_free = C::kTS ? (nq < 1 || mbar_try_wait(bar(B_SEMPTY0), (nq - 1) & 1))
+                                   : (nq < 2 || mbar_try_wait(bar(B_SEMPTY0 + (nq & 1)),
+                                                              ((nq >> 1) - 1) & 1));
         if (nq < nb && nq <= np + 1 && mbar_try_wait(bar(B_FULL0 + (nq & 1)), (nq >> 1) & 1) &&
-            (nq < 2 || mbar_try_wait(bar(B_SEMPTY0 + (nq & 1)), ((nq >> 1) - 1) & 1))) {
+            s_free) {
           tc_fence_after();
           opaque();
           ok = qk(nq);
           ++nq;
           t_idle = clock64();
-        } else if (np < nq && mbar_try_wait(bar(B_PFULL), np & 1)) {
+        } else if (np < nq && (C::kTS ? mbar_try_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
+                                      : mbar_try_wait(bar(B_PFULL0), np & 1))) {
           tc_fence_after();
           opaque();
           ok = pv(np);
@@ -614,13 +652,199 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
     }
     // the bulk copy of q has landed before the CTA can leave
-    if (warp == kMmaWarp && lane == 0 && nb > 0)
+    if (!C::kTS && warp == kMmaWarp && lane == 0 && nb > 0)
       mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
     // the cluster barrier of the merging epilogue, in step with the other roles
     if constexpr (MODE == kMergeL2) cluster_sync();
   } else if (warp < kSoftWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft) : "memory");
+    if constexpr (C::kTS) {
+    // ===================== softmax, Q in tensor memory (64 heads) =====================
+    // Thread tid owns tensor-memory lane tid: head h = tid % 64 and the half of the
+    // q/k columns (tid / 64) whose partial scores that lane accumulates.  The two
+    // threads of a head trade the partial scores of each other's tokens through X and
+    // each finishes 32 tokens of the block: thread (h, 0) tokens 0..31, (h, 1) 32..63.
+    // The running max of head h lives in a register of both threads.
+    const int h = tid & 63, half = tid >> 6;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int partner = tid ^ 64;
+    const bool poller = tid == 0;
+    bool ok = nb > 0;
+    if (ok) {
+      // ---- q row h, columns 256 half .. +255 (bf16) -> f16 pairs in columns 0..127 of
+      // this lane: the stacked Q operand; then the constant block of the value product
+      const uint4* src = reinterpret_cast<const uint4*>(
+          q + (static_cast<int64_t>(b) * H + h0 + h) * kQkDim + 256 * half);
+      bool q_bad = false;
+      uint4 c4[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c4[k] = ldg_nc_u4(src + k);
+#pragma unroll 1
+      for (int ph = 0; ph < 4; ++ph) {
+        uint4 n4[8];
+        if (ph < 3) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) n4[k] = ldg_nc_u4(src + 8 * (ph + 1) + k);
+        }
+        float f[32];   // column 32 ph + j: elements 2j, 2j + 1 of the chunk (f16 pair)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t w[4] = {c4[k].x, c4[k].y, c4[k].z, c4[k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t hv = bf16x2_to_f16x2(w[j]);
+            q_bad |= f16x2_has_inf_or_nan(hv);
+            f[4 * k + j] = __uint_as_float(hv);
+          }
+        }
+        tmem_st16(tQ + lane_base + 32 * ph, f);
+        tmem_st16(tQ + lane_base + 32 * ph + 16, f + 16);
+        if (ph < 3) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) c4[k] = n4[k];
+        }
+      }
+      tmem_wait_st();
+      if (q_bad) record_status(SMLA_ERR_RANGE);
+      {   // the constant block: 16 rows x 8 units of 16 B, column 0 = f16 1.0
+        const uint32_t r = tid >> 3, unit = tid & 7;
+        st_shared_v4(sbase + C::kOnesOff + (r >> 3) * 1024 + swz_offset(r & 7, unit, 128),
+                     make_uint4(unit == 0 ? 0x3C00u : 0u, 0u, 0u, 0u));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QREADY));
+    }
+    const int pair_bar = kBarPair0 + (warp & 1);   // warps w and w + 2 hold the two halves
+    const int tok0 = 32 * half;
+    // score columns: half 0 holds tokens 0..63 at 0..63, half 1 at 64..127; each
+    // thread keeps its own tokens and sends the partner's
+    const uint32_t send_col = half ? 64u : 32u, keep_col = half ? 96u : 0u;
+    // X row r (128 bytes) receives the 32 partial scores for thread r, 16-byte units
+    // XOR-swizzled with r so that 8 consecutive rows use 8 distinct bank groups
+    const uint32_t xw = sbase + C::kXOff + static_cast<uint32_t>(partner) * 128;
+    const uint32_t xr = sbase + C::kXOff + static_cast<uint32_t>(tid) * 128;
+    const uint32_t xsw = static_cast<uint32_t>(partner & 7), xsr = static_cast<uint32_t>(tid & 7);
+    float* mx = reinterpret_cast<float*>(smem + C::kMxOff);
+    float* alph = reinterpret_cast<float*>(smem + C::kAlphaOff);
+    float m_run = 0.f;     // running max of head h (log2 units), once have_m
+    bool have_m = false;   // a valid token has been seen (every head gets it at once)
+    int vraw = ok ? raw_idx(idx_row, sp.t_begin + tok0 + lane, sp.t_end) : -1;
+    for (int i = 0; ok && i < nb; ++i) {
+      // validity of this thread's 32 tokens: lane j tests token tok0 + j
+      const uint32_t vm = __ballot_sync(0xffffffffu, idx_ok(vraw, num_rows, false));
+      vraw = i + 1 < nb ? raw_idx(idx_row, sp.t_begin + (i + 1) * kBlk + tok0 + lane, sp.t_end)
+                        : -1;
+      bool wok = warp_wait(bar(B_SFULL0), i & 1, abort_f, limit);
+      float sv[32];
+      if (wok) {
+        tc_fence_after();
+        float x[32];
+        tmem_ld16(tS + lane_base + send_col, x);
+        tmem_ld16(tS + lane_base + send_col + 16, x + 16);
+        tmem_ld16(tS + lane_base + keep_col, sv);
+        tmem_ld16(tS + lane_base + keep_col + 16, sv + 16);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SEMPTY0));   // the scores may be rewritten
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(xw + ((static_cast<uint32_t>(k) ^ xsw) << 4),
+                       make_uint4(__float_as_uint(x[4 * k]), __float_as_uint(x[4 * k + 1]),
+                                  __float_as_uint(x[4 * k + 2]), __float_as_uint(x[4 * k + 3])));
+      }
+      wok = bar_and(pair_bar, 64, wok);   // both threads of every head have written X
+      // t = score * scale (log2 units) - running max (0 until the first valid token);
+      // masked tokens -inf.  ex: max of t over this thread's tokens; bm: the same before
+      // the running max is subtracted.
+      float ex = -INFINITY, bm = -INFINITY;
+      if (wok) {
+        const float base = have_m ? m_run : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = ld_shared_v4(xr + ((static_cast<uint32_t>(k) ^ xsr) << 4));
+          sv[4 * k] = fmaf(sv[4 * k] + __uint_as_float(v.x), scale_log2, -base);
+          sv[4 * k + 1] = fmaf(sv[4 * k + 1] + __uint_as_float(v.y), scale_log2, -base);
+          sv[4 * k + 2] = fmaf(sv[4 * k + 2] + __uint_as_float(v.z), scale_log2, -base);
+          sv[4 * k + 3] = fmaf(sv[4 * k + 3] + __uint_as_float(v.w), scale_log2, -base);
+        }
+        float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          if (!((vm >> t) & 1u)) sv[t] = -INFINITY;
+          e4[t & 3] = fmaxf(e4[t & 3], sv[t]);
+        }
+        ex = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
+        bm = ex + base;
+        if (!have_m && vm != 0u) ex = INFINITY;   // the first valid token sets the max
+      }
+      // One barrier in the common case: no score passed the running max by more than
+      // the headroom.
+      if (bar_or(kBarSoft, 128, !wok || ex > kLazyMax)) {
+        if (!(ok = bar_and(kBarSoft, 128, wok))) break;   // a wait ran out: leave together
+        // the new running max of head h: the old one and both threads' block maxima
+        // (finite: a valid token of this block or an earlier one exists)
+        mx[tid] = bm;
+        bar_sync(kBarSoft, 128);
+        const float m_new = fmaxf(have_m ? m_run : -INFINITY, fmaxf(bm, mx[partner]));
+        if (have_m) {
+          // rescale O (and with it the denominator row) by 2^(m_old - m_new), once the
+          // value product of block i - 1 has finished
+          if (tid < NH) alph[tid] = exp2f(m_run - m_new);
+          if (!(ok = group_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f,
+                                limit, poller, kBarSoft, 128)))
+            break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int hc = 0; hc < NH; hc += 8) {
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = alph[hc + k];
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+              float o[8];
+              tmem_ld<8>(tO + lane_base + mb * NH + hc, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 8; ++k) o[k] *= f[k];
+              tmem_st<8>(tO + lane_base + mb * NH + hc, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        const float d = m_new - (have_m ? m_run : 0.f);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) sv[t] -= d;
+        m_run = m_new;
+        have_m = true;
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) sv[t] = fast_exp2(sv[t]);   // 2^-inf = 0 (masked)
+      // P buffer i & 1 is free once the value product of block i - 2 has read it
+      if (i < 2 || warp_wait(bar(B_EMPTY0 + (i & 1)), ((i >> 1) & 1) ^ 1, abort_f, limit)) {
+        // row h of P (128 bytes: tokens 0..63), 16-byte units XOR-swizzled with h & 7
+        const uint32_t prow = sbase + C::kPOff + (i & 1) * C::kPStride +
+                              static_cast<uint32_t>((h >> 3) * 1024 + (h & 7) * 128);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 v;
+          v.x = pack_f16x2(sv[8 * k + 0], sv[8 * k + 1]);
+          v.y = pack_f16x2(sv[8 * k + 2], sv[8 * k + 3]);
+          v.z = pack_f16x2(sv[8 * k + 4], sv[8 * k + 5]);
+          v.w = pack_f16x2(sv[8 * k + 6], sv[8 * k + 7]);
+          st_shared_v4(prow + ((static_cast<uint32_t>(4 * half + k) ^ static_cast<uint32_t>(h & 7)) << 4), v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL0 + (i & 1)));
+      }
+    }
+    // the final running max into mbuf[0, NH) for the epilogue
+    if (tid < NH) mbuf[tid] = have_m ? m_run : 0.f;
+    } else {
     // ===================== softmax (and q conversion) =====================
     const int t = tid & (kBlk - 1);          // token of the block (tensor-memory lane tid)
     const bool upper = tid >= kBlk;          // this lane holds the columns 256..511 half
@@ -800,12 +1024,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL));
+        if (lane == 0) mbar_arrive(bar(B_PFULL0));
       }
     }
     // the final running max into mbuf[0, NH) for the epilogue
     bar_sync(kBarSoft, 128);
     if (cur == 1 && tid < NH) mbuf[tid] = mbuf[NH + tid];
+    }
     bar_sync(kBarEpi, kSoftWarps * 32 + kConv);
     if constexpr (MODE == kMergeL2) cluster_sync();
   } else {
@@ -897,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer u is free once the value product of block i - 2 is done; buffer 1
       // first holds the staged q rows until the softmax warps have converted them
       if (i >= 2) ok = warp_wait(bar(B_EMPTY0 + u), ((i >> 1) & 1) ^ 1, abort_f, limit);
-      else if (i == 1) ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
+      else if (i == 1 && !C::kTS) ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
       if (!ok) break;
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {

@@ -153,6 +153,20 @@ __device__ __forceinline__ void mma_f16_ss_hl(uint32_t d_tmem, uint32_t a_lo, ui
       : "memory");
 }
 
+// D (tensor memory) (+)= A . B with A read from tensor memory (M rows in M lanes,
+// K elements packed two f16 per 32-bit column, the even element in the low half)
+// and B from shared memory (descriptor as 32-bit halves).
+__device__ __forceinline__ void mma_f16_ts_hl(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on the mbarrier when all previously issued tcgen05.mma of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
