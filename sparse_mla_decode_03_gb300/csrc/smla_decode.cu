@@ -352,7 +352,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    __nanosleep(32);   // a waiting warp leaves the issue slots to the warps at work
     if (*abort_f) return false;
     if (clock64() - t0 > (static_cast<long long>(limit_k) << 10)) {
       *abort_f = 1;
@@ -611,26 +610,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Issue order decided by readiness: the scores of block nq (its buffer filled,
       // its scores buffer read by the softmax of block nq - 2; at most one block ahead
       // of the value products) or the value product of block np (its P written).  Each
-      // barrier is tested without blocking, so a late converter set or a late softmax
-      // holds up only its own block.
+      // barrier is tested without suspending (test_wait), so a late converter set or a
+      // late softmax holds up only its own block.
       int nq = 0, np = 0;
       long long t_idle = clock64();
 #pragma unroll 1
       while (ok && np < nb) {
         // scores buffer free: SS two buffers (read by the softmax of block nq - 2), TS
         // one (read by the softmax of block nq - 1)
-        const bool s_free = C::kTS ? (nq < 1 || mbar_try_wait(bar(B_SEMPTY0), (nq - 1) & 1))
-                                   : (nq < 2 || mbar_try_wait(bar(B_SEMPTY0 + (nq & 1)),
+        const bool s_free = C::kTS ? (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))
+                                   : (nq < 2 || mbar_test_wait(bar(B_SEMPTY0 + (nq & 1)),
                                                               ((nq >> 1) - 1) & 1));
-        if (nq < nb && nq <= np + 1 && mbar_try_wait(bar(B_FULL0 + (nq & 1)), (nq >> 1) & 1) &&
+        if (nq < nb && nq <= np + 1 && mbar_test_wait(bar(B_FULL0 + (nq & 1)), (nq >> 1) & 1) &&
             s_free) {
           tc_fence_after();
           opaque();
           ok = qk(nq);
           ++nq;
           t_idle = clock64();
-        } else if (np < nq && (C::kTS ? mbar_try_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
-                                      : mbar_try_wait(bar(B_PFULL0), np & 1))) {
+        } else if (np < nq && (C::kTS ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
+                                      : mbar_test_wait(bar(B_PFULL0), np & 1))) {
           tc_fence_after();
           opaque();
           ok = pv(np);
@@ -639,7 +638,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (*abort_f) {
           ok = false;
         } else if (clock64() - t_idle <= (static_cast<long long>(limit) << 10)) {
-          __nanosleep(20);   // nothing ready: yield the issue slots to the warps at work
         } else {
           *abort_f = 1;
           record_status(SMLA_ERR_TIMEOUT);
@@ -1066,7 +1064,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < 2; ++g)
         nraw[g] = raw_idx(idx_row, sp.t_begin + set * kBlk + rb0 + 4 * g, sp.t_end);
-      load_rows(set);
+      // Every CTA starts at once: block 0's rows are requested alone first, so they
+      // are not interleaved with block 1's in the memory queues; set 1 issues its
+      // first loads once block 0 is converted.
+      if (set == 1) ok = warp_wait(bar(B_FULL0), 0, abort_f, limit);
+      if (ok) load_rows(set);
     }
     // Word q + 8k (k < 7) of row r lands in slab k & 3, row r + 64 (k >> 2), 16-byte
     // unit q (XOR-swizzled with the row): this lane's base plus a compile-time offset.

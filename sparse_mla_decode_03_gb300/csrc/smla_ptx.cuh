@@ -35,6 +35,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (test_wait never suspends the thread, unlike
+// try_wait, which may wait a hardware-defined time for the phase): for a thread that
+// polls several barriers and must act on whichever completes first.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The same test, letting the hardware suspend the thread for up to `ns` nanoseconds
 // while the phase is incomplete (it resumes as soon as the phase completes), so a
 // waiting thread takes no issue slots from the warps doing work.
