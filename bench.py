@@ -638,7 +638,10 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "dtype_detail": "tensor-core operands f16 (FP8 e4m3 nope dequantised exactly, bf16 "
+                        "q and rope converted), fp32 accumulation and softmax; inputs FP8/bf16, "
+                        "output bf16 + fp32 lse",
         "config": config_dict(w, S, fused, timing),
         "gathered_kv_gbs": ws * mean_valid_bytes / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
@@ -656,7 +659,7 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": Ke,
                 "how": e2e_how},
-        "gpu_launches": K * (1 if fused else 3),
+        "gpu_launches": K * (1 if fused else 2),   # per step: fused, or split + combine
         "context": {"isolated_ms_per_step": iso_ms,
                     "isolated": "one step alone: L2 flushed before it, events around a "
                                 "single-step graph replay (includes the whole launch latency)",
