@@ -99,8 +99,9 @@ int smla_workspace_size(const smla_params* p, int32_t num_splits, size_t* bytes)
 /* How sparse_mla_decode runs for `p` with `num_splits` splits (0 = the default plan)
  * on the current device: *splits receives the resolved split count; *fused is 1 when
  * the splits of each (query, head group) run as one thread-block cluster that also
- * merges them (one launch: each split writes its partials to the workspace, and
- * after a cluster barrier each CTA merges a slice of the heads), 0 when a separate
+ * merges them (one launch: each split keeps its partial in its shared memory, and
+ * after a cluster barrier each CTA merges a slice of the heads, reading the other
+ * splits' partials through distributed shared memory), 0 when a separate
  * combine kernel merges them.  Either way this is the split-K scheme of "The 80KB
  * Mystery: Resolving Contradictory Evidence in Triton Kernel Optimization", section
  * "The Context: Optimizing Attention on Blackwell".  Clusters need splits <= 8 and
@@ -110,7 +111,8 @@ int smla_decode_plan(const smla_params* p, int32_t num_splits, int32_t* splits, 
 /*
  * One whole decode step: the split-K attention and the merge of its splits, as one
  * clustered launch when smla_decode_plan reports fused, else split + combine kernels
- * (the workspace holds the split partials in both cases).
+ * (the workspace holds the split partials for the combine kernel; the clustered
+ * launch merges on chip and leaves it untouched).
  *   q          bf16  [B, H, 512]  (448 nope | 64 rope), 16-byte aligned
  *   kv_cache   uint8 [num_rows, kv_row_stride], 16-byte aligned, rows as above
  *   indices    int32 [B, topk]    row ids; < 0 = masked slot (shared by all heads)

@@ -654,7 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
     // the cluster barrier of the merging epilogue, in step with the other roles
-    if constexpr (MODE == kMergeL2) cluster_sync();
+    // the two cluster barriers of the merging epilogue, in step with the other roles
+    if constexpr (MODE == kMergeL2) {
+      cluster_sync();
+      cluster_sync();
+    }
   } else if (warp < kSoftWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft) : "memory");
     if constexpr (C::kTS) {
@@ -1030,7 +1034,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (cur == 1 && tid < NH) mbuf[tid] = mbuf[NH + tid];
     }
     bar_sync(kBarEpi, kSoftWarps * 32 + kConv);
-    if constexpr (MODE == kMergeL2) cluster_sync();
+    // the two cluster barriers of the merging epilogue, in step with the other roles
+    if constexpr (MODE == kMergeL2) {
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConv) : "memory");
     // ===================== converters =====================
@@ -1146,63 +1154,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have_o) tc_fence_after();
     bar_sync(kBarEpi, kSoftWarps * 32 + kConv);   // the softmax's final max is in mbuf
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    if (cw == 2) {
-      // row 448 of value block 3 (tensor-memory lane 64: lane 0 of quarter 2) is
-      // sum_t P[t] per head
-#pragma unroll 1
-      for (int hc = 0; hc < NH; hc += 8) {
-        float o[8];
-        if (have_o) {
-          tmem_ld<8>(tO + lane_base + 3 * NH + hc, o);
-          tmem_wait_ld();
-        }
-        if (lane == 0) {
+    // Clustered launch: the block buffers (free once every MMA is done) hold this
+    // split's partial o_s [NH][448] (not yet divided by the denominators), its lse_s
+    // [NH] and 1/denominator rinv_s [NH], which the other splits of the cluster read,
+    // and the merge weights of the heads this CTA merges.
+    float* o_s = reinterpret_cast<float*>(smem);
+    float* lse_s = o_s + NH * kNope;
+    float* rinv_s = lse_s + NH;
+    float* wgt = rinv_s + NH;                // [NH][kMaxCluster]
+    float* fin = wgt + NH * kMaxCluster;     // [NH] final lse (natural log)
+    const uint32_t o_s_addr = sbase, lse_s_addr = sbase + 4u * NH * kNope,
+                   rinv_s_addr = lse_s_addr + 4u * NH;
+    // Warp (value block mb, quarter qd) holds O^T rows 128 mb + 32 qd + lane: value
+    // column d, all NH heads, in one batch of tensor-memory loads.  Row 448 (block 3,
+    // quarter 2, lane 0) is sum_t P[t], the denominators.
+    const int mb = cw >> 2;
+    const int d = mb * 128 + (warp & 3) * 32 + lane;
+    float o[NH];
+    if (have_o) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) lfin[hc + k] = have_o ? o[k] : 0.f;
-        }
+      for (int cc = 0; cc < NH / 16; ++cc) tmem_ld16(tO + lane_base + mb * NH + 16 * cc, o + 16 * cc);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int k = 0; k < NH; ++k) o[k] = 0.f;
+    }
+    if (d == kNope) {
+#pragma unroll
+      for (int k = 0; k < NH; ++k) lfin[k] = o[k];
+    }
+    if constexpr (MODE == kMergeL2) {
+      if (d < kNope) {
+#pragma unroll
+        for (int k = 0; k < NH; ++k) o_s[k * kNope + d] = o[k];
       }
     }
     bar_sync(kBarConv, kConv);
     if (wt < NH) {
       const float lt = lfin[wt];
       const float lse = lt > 0.f ? (mbuf[wt] + log2f(lt)) * kLn2 : -INFINITY;
-      lse_part[(static_cast<int64_t>(b) * H + h0 + wt) * S + s] = lse;
-      rinv[wt] = lt > 0.f ? 1.0f / lt : 0.f;
+      const float ri = lt > 0.f ? 1.0f / lt : 0.f;
+      if constexpr (MODE == kMergeL2) {   // read by the other splits of the cluster
+        lse_s[wt] = lse;
+        rinv_s[wt] = ri;
+      } else {
+        lse_part[(static_cast<int64_t>(b) * H + h0 + wt) * S + s] = lse;
+        rinv[wt] = ri;
+      }
     }
-    bar_sync(kBarConv, kConv);
-    {
-      // warp (value block mb, quarter qd) writes value rows 128 mb + 32 qd + lane
-      const int mb = cw >> 2;
-      const int d = mb * 128 + (warp & 3) * 32 + lane;
-      const int64_t hstride = static_cast<int64_t>(S) * kNope;
-      float* dst = o_part + ((static_cast<int64_t>(b) * H + h0) * S + s) * kNope + d;
-#pragma unroll 1
-      for (int cc = 0; cc < NH / 16; ++cc) {
-        float o[16];
-        if (have_o) {
-          tmem_ld16(tO + lane_base + mb * NH + 16 * cc, o);
-          tmem_wait_ld();
-        } else {
+    if constexpr (MODE != kMergeL2) {
+      bar_sync(kBarConv, kConv);
+      if (d < kNope) {
+        const int64_t hstride = static_cast<int64_t>(S) * kNope;
+        float* dst = o_part + ((static_cast<int64_t>(b) * H + h0) * S + s) * kNope + d;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = 0.f;
-        }
-        if (d < kNope) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) dst[(16 * cc + k) * hstride] = o[k] * rinv[16 * cc + k];
-        }
+        for (int k = 0; k < NH; ++k) dst[k * hstride] = o[k] * rinv[k];
       }
     }
     if constexpr (MODE == kMergeL2) {
-      cluster_sync();   // every split of this (query, head group) has written its partials
-      // this CTA merges heads [h_lo, h_hi): weights exp(lse_s - lse) per head first
+      cluster_sync();   // every split of this (query, head group) holds its partial
+      // This CTA merges heads [h_lo, h_hi), reading the other splits' partials from
+      // their shared memory (split r is cluster rank r): weights exp(lse_r - lse) / l_r.
       const int h_lo = s * NH / S, h_hi = (s + 1) * NH / S, nh = h_hi - h_lo;
-      float* wgt = reinterpret_cast<float*>(smem);   // [nh][kMaxCluster] (block buffer 0 is free)
-      float* fin = wgt + NH * kMaxCluster;           // [nh] final lse (natural log)
       if (wt < nh) {
-        const float* lp = lse_part + (static_cast<int64_t>(b) * H + h0 + h_lo + wt) * S;
-        float x[kMaxCluster];
+        float x[kMaxCluster], ri[kMaxCluster];
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) x[r] = r < S ? __ldcg(lp + r) : -INFINITY;
+        for (int r = 0; r < kMaxCluster; ++r) {
+          const uint32_t off = 4u * static_cast<uint32_t>(h_lo + wt);
+          x[r] = r < S ? ld_dsmem_f32(dsmem_addr(lse_s_addr + off, static_cast<uint32_t>(r)))
+                       : -INFINITY;
+          ri[r] = r < S ? ld_dsmem_f32(dsmem_addr(rinv_s_addr + off, static_cast<uint32_t>(r))) : 0.f;
+        }
         float M = -INFINITY;
 #pragma unroll
         for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, x[r]);
@@ -1215,43 +1237,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float inv = sum > 0.f ? 1.f / sum : 0.f;
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) wgt[wt * kMaxCluster + r] = x[r] * inv;
+        for (int r = 0; r < kMaxCluster; ++r) wgt[wt * kMaxCluster + r] = x[r] * inv * ri[r];
         fin[wt] = sum > 0.f ? M + logf(sum) : -INFINITY;
       }
       bar_sync(kBarConv, kConv);
       const int units = nh * (kNope / 4);
-      for (int uu = wt; uu < units; uu += kConv) {
-        const int hl = uu / (kNope / 4), d4 = uu % (kNope / 4);
-        const float4* src = reinterpret_cast<const float4*>(
-                                o_part + ((static_cast<int64_t>(b) * H + h0 + h_lo + hl) * S) * kNope) +
-                            d4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      // two units of 4 value columns per thread and round, so that 2 S loads from the
+      // other CTAs' shared memory are in flight together
+      for (int u0 = wt; u0 < units; u0 += 2 * kConv) {
+        bool act[2];
+        int hl[2], d4[2];
+        uint32_t src[2];
+        float4 acc[2];
 #pragma unroll
-        for (int r0 = 0; r0 < kMaxCluster; r0 += 4) {   // four splits' loads in flight
-          float4 v[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r0 + r < S) v[r] = __ldcg(src + (r0 + r) * (kNope / 4));
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            if (r0 + r < S) {
-              const float ws = wgt[hl * kMaxCluster + r0 + r];
-              acc.x = fmaf(ws, v[r].x, acc.x);
-              acc.y = fmaf(ws, v[r].y, acc.y);
-              acc.z = fmaf(ws, v[r].z, acc.z);
-              acc.w = fmaf(ws, v[r].w, acc.w);
-            }
-          }
+        for (int j = 0; j < 2; ++j) {
+          const int uu = u0 + j * kConv;
+          act[j] = uu < units;
+          hl[j] = act[j] ? uu / (kNope / 4) : 0;
+          d4[j] = act[j] ? uu % (kNope / 4) : 0;
+          src[j] = o_s_addr + 4u * static_cast<uint32_t>((h_lo + hl[j]) * kNope + 4 * d4[j]);
+          acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 pk;
-        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * H + h0 + h_lo + hl) * kNope +
-                                  4 * d4) = pk;
+#pragma unroll
+        for (int r0 = 0; r0 < kMaxCluster; r0 += 4) {
+          float4 v[2][4];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              if (act[j] && r0 + r < S) v[j][r] = ld_dsmem_v4(dsmem_addr(src[j], static_cast<uint32_t>(r0 + r)));
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              if (act[j] && r0 + r < S) {
+                const float ws = wgt[hl[j] * kMaxCluster + r0 + r];
+                acc[j].x = fmaf(ws, v[j][r].x, acc[j].x);
+                acc[j].y = fmaf(ws, v[j][r].y, acc[j].y);
+                acc[j].z = fmaf(ws, v[j][r].z, acc[j].z);
+                acc[j].w = fmaf(ws, v[j][r].w, acc[j].w);
+              }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (!act[j]) continue;
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x, acc[j].y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z, acc[j].w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * H + h0 + h_lo + hl[j]) * kNope +
+                                    4 * d4[j]) = pk;
+        }
       }
       if (wt < nh) lse_out[static_cast<int64_t>(b) * H + h0 + h_lo + wt] = fin[wt];
+      cluster_sync();   // the other splits have finished reading this CTA's shared memory
     }
   }
   tc_fence_before();
