@@ -101,15 +101,17 @@ enum : int { kSplitOnly = 0, kMergeL2 = 1 };
 // Named barriers (id 0 is __syncthreads).
 enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 = 5 };
 
-// mbarriers.  FULL0/1: block buffer filled (one arrival per converter warp);
-// EMPTY0/1: value product of the block in that buffer done (buffer and P free);
+// mbarriers.  FULL0..2: block buffer filled (one arrival per converter warp of the
+// set that fills it); EMPTY0..2: value product of the block in that buffer done
+// (buffer and, with one P buffer, P free);
 // SFULL0/1: scores in tensor-memory buffer 0/1 (one buffer, SFULL0, with Q in tensor
 // memory); SEMPTY0/1: softmax has read them; PFULL0/1: P buffer 0/1 written (one
 // buffer, PFULL0, with Q in shared memory); ODONE: all MMAs done; QRAW: the bf16 q
 // rows copied into buffer 1 (Q in shared memory); QREADY: the stacked f16 Q and the
 // constant block written.
 enum Bar : int {
-  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1,
+  B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_SFULL0, B_SFULL1,
+  B_SEMPTY0, B_SEMPTY1,
   B_PFULL0, B_PFULL1, B_ODONE, B_QRAW, B_QREADY, B_COUNT
 };
 
@@ -121,14 +123,20 @@ struct Cfg {
   static constexpr bool kTS = NH == 64;
   static constexpr int kHalf = NH / 2;                     // heads per softmax thread (SS)
   static constexpr int kQSlab = 2 * NH * 128;              // stacked Q: 2 NH rows x 128 B
-  static constexpr int kQOff = 2 * kBuf;
+  // Two block buffers.  (A third fits for 16 and 64 heads, but above ~195 KB of shared
+  // memory the carve-out leaves L1 too small for the row gathers: measured slower.)
+  static constexpr int kNBuf = 2;
+  static constexpr int kQOff = kNBuf * kBuf;
   // P: SS [64 tokens][NH] (MN-major B operand), one buffer; TS [NH heads][64 tokens]
-  // (K-major B operand, 128-byte rows), two buffers
-  static constexpr int kPOff = kTS ? 2 * kBuf : kQOff + 4 * kQSlab;
+  // (K-major B operand, 128-byte rows), two buffers with two block buffers, one with
+  // three (shared memory)
+  static constexpr int kPOff = kTS ? kNBuf * kBuf : kQOff + 4 * kQSlab;
   static constexpr int kPRow = 2 * NH;                     // bytes of one P row (SS: token)
   static constexpr int kPBytes = kBlk * kPRow;
   static constexpr int kPStride = ((kPBytes + 1023) / 1024) * 1024;
-  static constexpr int kPBufs = kTS ? 2 : 1;
+  // one P buffer: keeps the 64-head CTA under ~163 KB, where the carve-out leaves
+  // 92 KB of L1 for the row gathers
+  static constexpr int kPBufs = 1;
   static constexpr int kXOff = kPOff + kPBufs * kPStride;
   // SS: score halves traded, and the block-max transpose (NH heads x 65 floats);
   // TS: 32 partial scores per thread (128 rows of 128 bytes)
@@ -479,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
   if (tid == 0) {
-    mbar_init(bar(B_FULL0), kConvWarps / 2);   // one set of converter warps per buffer
-    mbar_init(bar(B_FULL1), kConvWarps / 2);
+    // one set of converter warps (8) fills each block
+    for (int i = B_FULL0; i <= B_FULL2; ++i) mbar_init(bar(i), kConvWarps / 2);
     for (int i = B_EMPTY0; i <= B_SFULL1; ++i) mbar_init(bar(i), 1);
     mbar_init(bar(B_SEMPTY0), kSoftWarps);
     mbar_init(bar(B_SEMPTY1), kSoftWarps);
@@ -562,8 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = wait(B_QREADY, 0);
       auto qk = [&](int i) {
-        const int u = i & 1;
-        const uint32_t aK = lK + static_cast<uint32_t>((u * kBuf) >> 4);
+        const int u = i & 1;                 // scores buffer (SS)
+        const int kb = i % C::kNBuf;         // block buffer
+        const uint32_t aK = lK + static_cast<uint32_t>((kb * kBuf) >> 4);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -583,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto pv = [&](int i) {
-        const int u = i & 1;
+        const int kb = i % C::kNBuf;                     // block buffer
+        const int pb = C::kPBufs == 2 ? (i & 1) : 0;     // P buffer
         const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int mb = 0; mb < 4; ++mb) {
@@ -591,19 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 4; ++ks) {
             uint32_t a;
             if (mb < 3) {
-              a = lK + lo_of(u * kBuf + (mb & 1) * 2 * kSlab + (mb >> 1) * 64 * 128 + ks * 2048,
+              a = lK + lo_of(kb * kBuf + (mb & 1) * 2 * kSlab + (mb >> 1) * 64 * 128 + ks * 2048,
                              kSlab);
             } else {
-              const uint32_t st = u * kBuf + kV3 + ks * 2048;
+              const uint32_t st = kb * kBuf + kV3 + ks * 2048;
               a = lK + lo_of(st, C::kOnesOff - st);
             }
             // K step of 16 tokens: SS 16 P rows down, TS 32 bytes along each P row
-            const uint32_t bP = C::kTS ? static_cast<uint32_t>((u * C::kPStride + ks * 32) >> 4)
+            const uint32_t bP = C::kTS ? static_cast<uint32_t>((pb * C::kPStride + ks * 32) >> 4)
                                        : static_cast<uint32_t>((ks * 16 * C::kPRow) >> 4);
             mma_f16_ss_hl(tO + mb * NH, a, hi, lP + bP, hiP, kIdescPV, ks > 0 ? 1u : acc0);
           }
         }
-        mma_commit(bar(B_EMPTY0 + u));
+        mma_commit(bar(B_EMPTY0 + kb));
         opaque();
         return true;
       };
@@ -621,15 +631,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool s_free = C::kTS ? (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))
                                    : (nq < 2 || mbar_test_wait(bar(B_SEMPTY0 + (nq & 1)),
                                                               ((nq >> 1) - 1) & 1));
-        if (nq < nb && nq <= np + 1 && mbar_test_wait(bar(B_FULL0 + (nq & 1)), (nq >> 1) & 1) &&
+        if (nq < nb && nq <= np + 1 &&
+            mbar_test_wait(bar(B_FULL0 + nq % C::kNBuf), (nq / C::kNBuf) & 1) &&
             s_free) {
           tc_fence_after();
           opaque();
           ok = qk(nq);
           ++nq;
           t_idle = clock64();
-        } else if (np < nq && (C::kTS ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
-                                      : mbar_test_wait(bar(B_PFULL0), np & 1))) {
+        } else if (np < nq && (C::kPBufs == 2 ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
+                                              : mbar_test_wait(bar(B_PFULL0), np & 1))) {
           tc_fence_after();
           opaque();
           ok = pv(np);
@@ -796,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // rescale O (and with it the denominator row) by 2^(m_old - m_new), once the
           // value product of block i - 1 has finished
           if (tid < NH) alph[tid] = exp2f(m_run - m_new);
-          if (!(ok = group_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f,
+          if (!(ok = group_wait(bar(B_EMPTY0 + (i - 1) % C::kNBuf), ((i - 1) / C::kNBuf) & 1, abort_f,
                                 limit, poller, kBarSoft, 128)))
             break;
           tc_fence_after();
@@ -825,10 +836,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int t = 0; t < 32; ++t) sv[t] = fast_exp2(sv[t]);   // 2^-inf = 0 (masked)
-      // P buffer i & 1 is free once the value product of block i - 2 has read it
-      if (i < 2 || warp_wait(bar(B_EMPTY0 + (i & 1)), ((i >> 1) & 1) ^ 1, abort_f, limit)) {
+      // P buffer pb is free once the value product that last read it (block i - kPBufs)
+      // has finished
+      const int pb = C::kPBufs == 2 ? (i & 1) : 0;
+      const int pj = i - C::kPBufs;
+      if (pj < 0 || warp_wait(bar(B_EMPTY0 + pj % C::kNBuf), (pj / C::kNBuf) & 1, abort_f, limit)) {
         // row h of P (128 bytes: tokens 0..63), 16-byte units XOR-swizzled with h & 7
-        const uint32_t prow = sbase + C::kPOff + (i & 1) * C::kPStride +
+        const uint32_t prow = sbase + C::kPOff + pb * C::kPStride +
                               static_cast<uint32_t>((h >> 3) * 1024 + (h & 7) * 128);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -841,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL0 + (i & 1)));
+        if (lane == 0) mbar_arrive(bar(B_PFULL0 + pb));
       }
     }
     // the final running max into mbuf[0, NH) for the epilogue
@@ -979,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bar_sync(kBarSoft, 128);
         if (have_m) {
           // O holds the value products up to block i - 1: let the last one finish
-          if (!(ok = group_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f,
+          if (!(ok = group_wait(bar(B_EMPTY0 + (i - 1) % C::kNBuf), ((i - 1) / C::kNBuf) & 1, abort_f,
                                 limit, poller, kBarSoft, 128)))
             break;
           tc_fence_after();
@@ -1012,7 +1026,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P is single-buffered: the value product of block i - 1 must have read it.  A
       // warp whose wait runs out skips its part of P; the abort flag it set makes the
       // next block's vote fire (or the MMA warp give up on this block's P).
-      if (i == 0 || warp_wait(bar(B_EMPTY0 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_f, limit)) {
+      if (i == 0 || warp_wait(bar(B_EMPTY0 + (i - 1) % C::kNBuf), ((i - 1) / C::kNBuf) & 1, abort_f,
+                              limit)) {
         const uint32_t prow = sbase + C::kPOff;   // row t: token-major, heads contiguous
 #pragma unroll
         for (int k = 0; k < HH / 8; ++k) {
@@ -1087,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto convert = [&](const uint2 (&d)[kSlots], int g, int i) {
       const uint32_t rx = rx0 ^ (4u * g);
       const uint32_t rowq = static_cast<uint32_t>(rb0 + 4 * g) * 128;
-      const uint32_t buf = sbase + (i & 1) * kBuf;
+      const uint32_t buf = sbase + (i % C::kNBuf) * kBuf;
       // scale word of this lane's row (word 56: slot 7 of lane q = 0)
       const uint32_t lo = __shfl_sync(0xffffffffu, d[7].x, row_lane0);
       const uint32_t hi = __shfl_sync(0xffffffffu, d[7].y, row_lane0);
@@ -1128,11 +1143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bad) record_status(SMLA_ERR_RANGE);
     };
     for (int i = set; ok && i < nb; i += 2) {
-      const int u = i & 1;
-      // buffer u is free once the value product of block i - 2 is done; buffer 1
-      // first holds the staged q rows until the softmax warps have converted them
-      if (i >= 2) ok = warp_wait(bar(B_EMPTY0 + u), ((i >> 1) & 1) ^ 1, abort_f, limit);
-      else if (i == 1 && !C::kTS) ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
+      const int u = i % C::kNBuf;
+      // buffer u is free once the value product of block i - kNBuf is done; buffer 1
+      // first holds the staged q rows (Q in shared memory) until the softmax warps
+      // have converted them
+      if (i >= C::kNBuf)
+        ok = warp_wait(bar(B_EMPTY0 + u), ((i / C::kNBuf) - 1) & 1, abort_f, limit);
+      else if (i == 1 && !C::kTS)
+        ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
       if (!ok) break;
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {
