@@ -45,8 +45,9 @@
 //   warps 0..3    softmax: one thread per tensor-memory lane; they also convert q
 //   warps 4..19   16 converters: each gathers, dequantises and stores 4 rows of a
 //                 block (8 lanes per row, 16-byte loads), and writes the epilogue
-//   warp 20       allocates tensor memory and issues every tcgen05.mma (one lane)
-//   warps 21..23  idle (their registers go to the other roles)
+//   warp 20       allocates tensor memory and issues the score MMAs (one lane)
+//   warp 21       issues the value-product MMAs (one lane)
+//   warps 22..23  idle (their registers go to the other roles)
 // Every wait is bounded; on timeout the CTA records SMLA_ERR_TIMEOUT in the device
 // status word and leaves through the epilogue.
 #include <cuda_bf16.h>
@@ -106,13 +107,14 @@ enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 =
 // (buffer and, with one P buffer, P free);
 // SFULL0/1: scores in tensor-memory buffer 0/1 (one buffer, SFULL0, with Q in tensor
 // memory); SEMPTY0/1: softmax has read them; PFULL0/1: P buffer 0/1 written (one
-// buffer, PFULL0, with Q in shared memory); ODONE: all MMAs done; QRAW: the bf16 q
+// buffer, PFULL0, with Q in shared memory); ODONE: all value products done (and with
+// them all scores); QDONE: the score MMAs done (drain on abort); QRAW: the bf16 q
 // rows copied into buffer 1 (Q in shared memory); QREADY: the stacked f16 Q and the
 // constant block written.
 enum Bar : int {
   B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_SFULL0, B_SFULL1,
   B_SEMPTY0, B_SEMPTY1,
-  B_PFULL0, B_PFULL1, B_ODONE, B_QRAW, B_QREADY, B_COUNT
+  B_PFULL0, B_PFULL1, B_ODONE, B_QDONE, B_QRAW, B_QREADY, B_COUNT
 };
 
 template <int NH>
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_PFULL0), kSoftWarps);
     mbar_init(bar(B_PFULL1), kSoftWarps);
     mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_QDONE), 1);
     mbar_init(bar(B_QRAW), 1);
     mbar_init(bar(B_QREADY), kSoftWarps);
     *abort_f = 0;
@@ -522,10 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kMmaWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma) : "memory");
     // ===================== MMA issuer =====================
-    if (warp == kMmaWarp && lane == 0 && nb > 0) {
+    // Q in shared memory: warp kMmaWarp issues the score MMAs, warp kMmaWarp + 1 the
+    // value products, each waiting (suspending) on its own barriers only.  Q in tensor
+    // memory (one scores buffer): warp kMmaWarp issues both in readiness order, which
+    // measured faster there (two issuers interleave a block's value product with the
+    // next block's scores in the tensor pipe and delay both).
+    constexpr bool kTwoIssuers = !C::kTS;
+    const bool qk_issuer = warp == kMmaWarp, pv_issuer = kTwoIssuers && warp == kMmaWarp + 1;
+    if ((qk_issuer || pv_issuer) && lane == 0 && nb > 0) {
       // SS: the bf16 q rows h0..h0+NH-1 (contiguous, NH KB) into block buffer 1, where
       // the softmax warps convert them into the stacked Q operand.
-      if constexpr (!C::kTS) {
+      if (!C::kTS && qk_issuer) {
         const uint8_t* src =
             reinterpret_cast<const uint8_t*>(q + (static_cast<int64_t>(b) * H + h0) * kQkDim);
         mbar_arrive_expect_tx(bar(B_QRAW), NH * 1024);
@@ -568,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         opaque();
         return r;
       };
-      bool ok = wait(B_QREADY, 0);
+      bool ok = true;
       auto qk = [&](int i) {
         const int u = i & 1;                 // scores buffer (SS)
         const int kb = i % C::kNBuf;         // block buffer
@@ -617,51 +627,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         opaque();
         return true;
       };
-      // Issue order decided by readiness: the scores of block nq (its buffer filled,
-      // its scores buffer read by the softmax of block nq - 2; at most one block ahead
-      // of the value products) or the value product of block np (its P written).  Each
-      // barrier is tested without suspending (test_wait), so a late converter set or a
-      // late softmax holds up only its own block.
-      int nq = 0, np = 0;
-      long long t_idle = clock64();
+      if (!kTwoIssuers) {
+        // Issue order decided by readiness: the scores of block nq (its buffer filled,
+        // the scores buffer read by the softmax of block nq - 1; at most one block
+        // ahead of the value products) or the value product of block np (its P
+        // written).  Each barrier is tested without suspending (test_wait), so a late
+        // converter set or a late softmax holds up only its own block.
+        ok = wait(B_QREADY, 0);
+        int nq = 0, np = 0;
+        long long t_idle = clock64();
 #pragma unroll 1
-      while (ok && np < nb) {
-        // scores buffer free: SS two buffers (read by the softmax of block nq - 2), TS
-        // one (read by the softmax of block nq - 1)
-        const bool s_free = C::kTS ? (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))
-                                   : (nq < 2 || mbar_test_wait(bar(B_SEMPTY0 + (nq & 1)),
-                                                              ((nq >> 1) - 1) & 1));
-        if (nq < nb && nq <= np + 1 &&
-            mbar_test_wait(bar(B_FULL0 + nq % C::kNBuf), (nq / C::kNBuf) & 1) &&
-            s_free) {
-          tc_fence_after();
-          opaque();
-          ok = qk(nq);
-          ++nq;
-          t_idle = clock64();
-        } else if (np < nq && (C::kPBufs == 2 ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
-                                              : mbar_test_wait(bar(B_PFULL0), np & 1))) {
-          tc_fence_after();
-          opaque();
-          ok = pv(np);
-          ++np;
-          t_idle = clock64();
-        } else if (*abort_f) {
-          ok = false;
-        } else if (clock64() - t_idle <= (static_cast<long long>(limit) << 10)) {
-        } else {
-          *abort_f = 1;
-          record_status(SMLA_ERR_TIMEOUT);
-          ok = false;
+        while (ok && np < nb) {
+          if (nq < nb && nq <= np + 1 &&
+              mbar_test_wait(bar(B_FULL0 + nq % C::kNBuf), (nq / C::kNBuf) & 1) &&
+              (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))) {
+            tc_fence_after();
+            opaque();
+            ok = qk(nq);
+            ++nq;
+            t_idle = clock64();
+          } else if (np < nq && (C::kPBufs == 2 ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
+                                                : mbar_test_wait(bar(B_PFULL0), np & 1))) {
+            tc_fence_after();
+            opaque();
+            ok = pv(np);
+            ++np;
+            t_idle = clock64();
+          } else if (*abort_f) {
+            ok = false;
+          } else if (clock64() - t_idle > (static_cast<long long>(limit) << 10)) {
+            *abort_f = 1;
+            record_status(SMLA_ERR_TIMEOUT);
+            ok = false;
+          }
         }
+        mma_commit(bar(B_ODONE));
+        // Let the tensor pipe drain before the final barrier (tensor memory is freed
+        // after it), also when another role left early.
+        if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
+      } else       if (qk_issuer) {
+        // scores of block i: its buffer filled, and its scores buffer read by the
+        // softmax (TS: one buffer, block i - 1; SS: two, block i - 2)
+        ok = wait(B_QREADY, 0);
+#pragma unroll 1
+        for (int i = 0; ok && i < nb; ++i) {
+          ok = wait(B_FULL0 + i % C::kNBuf, (i / C::kNBuf) & 1);
+          if (ok && C::kTS && i >= 1) ok = wait(B_SEMPTY0, (i - 1) & 1);
+          if (ok && !C::kTS && i >= 2) ok = wait(B_SEMPTY0 + (i & 1), ((i >> 1) - 1) & 1);
+          if (ok) ok = qk(i);
+        }
+        mma_commit(bar(B_QDONE));
+        // let the score MMAs drain before tensor memory is freed, also when another
+        // role left early
+        if (!ok) mbar_wait(bar(B_QDONE), 0, static_cast<long long>(kWaitLimitK) << 10);
+      } else {
+        // value product of block i: its P written (every earlier value product of the
+        // same accumulator was issued before by this thread)
+#pragma unroll 1
+        for (int i = 0; ok && i < nb; ++i) {
+          ok = C::kPBufs == 2 ? wait(B_PFULL0 + (i & 1), (i >> 1) & 1) : wait(B_PFULL0, i & 1);
+          if (ok) ok = pv(i);
+        }
+        mma_commit(bar(B_ODONE));
+        if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
       }
-      mma_commit(bar(B_ODONE));
-      // Let the tensor pipe drain before the final barrier (tensor memory is freed
-      // after it), also when another role left early.
-      if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
     }
     // the bulk copy of q has landed before the CTA can leave
-    if (!C::kTS && warp == kMmaWarp && lane == 0 && nb > 0)
+    if (!C::kTS && qk_issuer && lane == 0 && nb > 0)
       mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
     // the cluster barrier of the merging epilogue, in step with the other roles
