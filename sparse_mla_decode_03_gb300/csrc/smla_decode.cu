@@ -1162,17 +1162,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // rope: word 56 + q (slot 7, q >= 1), 64 + q (slot 8), 72 (slot 9, q = 0) is
       // rope word r = w - 57: f16 8 bytes at unit r / 2, half r % 2 of the rope row
-      bool bad = false;
+      // (range: a bf16 magnitude >= 0x4780 = 65536, or inf / NaN, is beyond the f16
+      // range; one 16-bit SIMD max of the magnitudes, tested once)
+      uint32_t mag = 0u;
       const uint32_t rope_base = buf + 3 * kSlab + 64 * 128 + rowq;
       auto rope = [&](int r, uint2 v2) {
+        mag = __vmaxu2(mag, __vmaxu2(v2.x & 0x7fff7fffu, v2.y & 0x7fff7fffu));
         const uint2 v = make_uint2(bf16x2_to_f16x2(v2.x), bf16x2_to_f16x2(v2.y));
-        bad |= f16x2_has_inf_or_nan(v.x) | f16x2_has_inf_or_nan(v.y);
         st_shared_v2(rope_base + (((static_cast<uint32_t>(r) >> 1) ^ rx) << 4) + (r & 1) * 8, v);
       };
       if (q8 >= 1) rope(q8 - 1, d[7]);
       rope(q8 + 7, d[8]);
       if (q8 == 0) rope(15, d[9]);
-      if (bad) record_status(SMLA_ERR_RANGE);
+      if (__vcmpgeu2(mag, 0x47804780u) != 0u) record_status(SMLA_ERR_RANGE);
     };
     for (int i = set; ok && i < nb; i += 2) {
       const int u = i % C::kNBuf;
@@ -1184,13 +1186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else if (i == 1 && !C::kTS)
         ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
       if (!ok) break;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        uint2 d[kSlots];
-#pragma unroll
-        for (int j = 0; j < kSlots; ++j) d[j] = g ? c[1][j] : c[0][j];
-        convert(d, g, i);
-      }
+      convert(c[0], 0, i);
+      convert(c[1], 1, i);
       fence_proxy_async_smem();
       __syncwarp();
       // (the test hook withholds one warp's arrival, so the MMA warp's wait runs out)

@@ -132,3 +132,21 @@ def test_q_beyond_f16_range_is_reported():
     _decode(q.to(torch.bfloat16).cuda(), kv, idx)
     assert smla_device_status(clear=True) == _lib.SMLA_ERR_RANGE
     assert smla_device_status() == 0
+
+
+@pytest.mark.parametrize("H", [16, 64])
+def test_rope_beyond_f16_range_is_reported(H):
+    """The rope part is bf16 and is converted to f16: a magnitude of 65536 (bf16 0x4780)
+    or more overflows f16 and sets SMLA_ERR_RANGE; 65280 (0x477F, the largest bf16
+    below it) converts exactly and does not."""
+    rows = build_rows(64, seed=9)
+    idx = np.arange(32, dtype=np.int32)[None]
+    q = torch.randn((1, H, 512), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    for bits, expect in ((0x477F, 0), (0xC77F, 0), (0x4780, _lib.SMLA_ERR_RANGE),
+                         (0xC780, _lib.SMLA_ERR_RANGE)):
+        r = rows.copy()
+        r[7, W.ROPE_OFF + 2 * 37:W.ROPE_OFF + 2 * 37 + 2] = np.array([bits & 0xFF, bits >> 8], np.uint8)
+        kv = torch.as_tensor(r, device="cuda")
+        smla_device_status(clear=True)
+        _decode(q, kv, idx)
+        assert smla_device_status(clear=True) == expect, hex(bits)
