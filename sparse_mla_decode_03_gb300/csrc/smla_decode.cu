@@ -816,12 +816,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           sv[4 * k + 2] = fmaf(sv[4 * k + 2] + __uint_as_float(v.z), scale_log2, -base);
           sv[4 * k + 3] = fmaf(sv[4 * k + 3] + __uint_as_float(v.w), scale_log2, -base);
         }
+        if (vm != 0xffffffffu) {   // (warp-uniform: the tokens are the warp's)
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (!((vm >> t) & 1u)) sv[t] = -INFINITY;
+        }
         float e4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          if (!((vm >> t) & 1u)) sv[t] = -INFINITY;
-          e4[t & 3] = fmaxf(e4[t & 3], sv[t]);
-        }
+        for (int t = 0; t < 32; ++t) e4[t & 3] = fmaxf(e4[t & 3], sv[t]);
         ex = fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
         bm = ex + base;
         if (!have_m && vm != 0u) ex = INFINITY;   // the first valid token sets the max
