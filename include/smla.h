@@ -74,6 +74,10 @@ enum smla_status {
                                        outside the f16 range of the tensor-core operands */
   SMLA_ERR_SCRATCH_TOO_SMALL = -9,  /* sparse_mla_decode_noalloc: the split partials need
                                        more than its built-in 16 MiB scratch */
+  SMLA_ERR_INTERNAL = -10,          /* device status, debug build (libsmla_debug.so, built
+                                       with SMLA_DEBUG) only: a computed shared-memory
+                                       address or gathered row fell outside its buffer;
+                                       the access was skipped */
 };
 
 /* Problem description shared by the entry points. */

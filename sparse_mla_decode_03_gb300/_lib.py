@@ -8,6 +8,8 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsmla.so")
+# the same library built with SMLA_DEBUG (device-side bounds checks; see build.py)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libsmla_debug.so")
 
 SMLA_OK = 0
 SMLA_ERR_INVALID_ARG = -1
@@ -19,6 +21,7 @@ SMLA_ERR_TIMEOUT = -6
 SMLA_ERR_INDEX_RANGE = -7
 SMLA_ERR_RANGE = -8
 SMLA_ERR_SCRATCH_TOO_SMALL = -9
+SMLA_ERR_INTERNAL = -10
 
 EXPORTED = (
     "smla_default_num_splits",
@@ -50,16 +53,29 @@ class SmlaParams(ctypes.Structure):
 
 
 _lib = None
+_debug_lib = None
 
 
 def load() -> ctypes.CDLL:
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
+    if _lib is None:
+        _lib = _open(LIB_PATH)
+    return _lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """The SMLA_DEBUG build of the same C ABI (a separate library and device state)."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _open(DEBUG_LIB_PATH)
+    return _debug_lib
+
+
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"{LIB_PATH} is missing: build it with `python -m sparse_mla_decode_03_gb300.build`")
-    lib = ctypes.CDLL(LIB_PATH)
+            f"{path} is missing: build it with `python -m sparse_mla_decode_03_gb300.build`")
+    lib = ctypes.CDLL(path)
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     P = ctypes.POINTER(SmlaParams)
     lib.smla_default_num_splits.argtypes = [P, ctypes.POINTER(i32)]
@@ -79,5 +95,4 @@ def load() -> ctypes.CDLL:
     for name in EXPORTED:
         if name != "smla_status_string":
             getattr(lib, name).restype = ctypes.c_int
-    _lib = lib
     return lib

@@ -363,6 +363,8 @@ const char* smla_status_string(int status) {
     case SMLA_ERR_RANGE: return "SMLA_ERR_RANGE: a q or KV value exceeds the f16 operand range";
     case SMLA_ERR_SCRATCH_TOO_SMALL:
       return "SMLA_ERR_SCRATCH_TOO_SMALL: split partials exceed the 16 MiB built-in scratch";
+    case SMLA_ERR_INTERNAL:
+      return "SMLA_ERR_INTERNAL: a debug-build bounds check failed (access skipped)";
     default: return "SMLA: unknown status";
   }
 }

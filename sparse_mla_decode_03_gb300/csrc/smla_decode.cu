@@ -165,13 +165,34 @@ struct Cfg {
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_smla_status, 0, code); }
 
+#ifdef SMLA_DEBUG
+// Debug build: every computed shared-memory address of the explicit shared loads and
+// stores is checked against this CTA's dynamic shared-memory window, and every
+// gathered row's byte range against the cache; a violation records
+// SMLA_ERR_INTERNAL in the device status word and the access is skipped (no trap).
+extern __shared__ uint8_t smla_dbg_dynamic_smem[];
+__device__ __forceinline__ bool smem_access_ok(uint32_t addr, uint32_t bytes) {
+  uint32_t size;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+  const uint32_t lo = smem_u32(smla_dbg_dynamic_smem);
+  const bool ok = addr >= lo && addr + bytes <= lo + size;
+  if (!ok) record_status(SMLA_ERR_INTERNAL);
+  return ok;
+}
+#define SMLA_SMEM_OK(addr, bytes) smem_access_ok((addr), (bytes))
+#else
+#define SMLA_SMEM_OK(addr, bytes) true
+#endif
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  if (!SMLA_SMEM_OK(addr, 16)) return;
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
+  if (!SMLA_SMEM_OK(addr, 16)) return make_uint4(0u, 0u, 0u, 0u);
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr)
@@ -179,6 +200,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
+  if (!SMLA_SMEM_OK(addr, 8)) return;
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
 }
 __device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
@@ -1105,7 +1127,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nraw[2] = {-1, -1};                      // stored indices of the rows, 2 blocks ahead
     bool ok = set < nb;
     auto row_of = [&](int raw, bool report) -> const uint8_t* {
-      return idx_ok(raw, num_rows, report) ? kv + static_cast<int64_t>(raw) * stride : nullptr;
+      if (!idx_ok(raw, num_rows, report)) return nullptr;
+#ifdef SMLA_DEBUG
+      // the row's 584 bytes lie inside the cache
+      if (static_cast<int64_t>(raw) * stride + kRowBytes > num_rows * stride) {
+        record_status(SMLA_ERR_INTERNAL);
+        return nullptr;
+      }
+#endif
+      return kv + static_cast<int64_t>(raw) * stride;
     };
     auto load_rows = [&](int i) {   // rows of block i (nraw) into c; indices of block i + 2
 #pragma unroll

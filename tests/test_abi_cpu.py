@@ -38,8 +38,15 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(_lib.EXPORTED) <= names
 
 
+def test_debug_build_exports_the_same_abi(lib):
+    dbg = _lib.load_debug()
+    for n in declared_functions():
+        assert hasattr(dbg, n), f"{n} not exported by the SMLA_DEBUG build"
+    assert "SMLA_ERR_INTERNAL" in dbg.smla_status_string(_lib.SMLA_ERR_INTERNAL).decode()
+
+
 def test_status_strings(lib):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = lib.smla_status_string(code).decode()
         assert s.startswith("SMLA")
     assert "unknown" in lib.smla_status_string(-99).decode()
