@@ -62,23 +62,29 @@ int max_splits(const smla_params* p) {
 }
 
 // Step time model, in units of one 64-slot block of a CTA (one CTA per SM is
-// resident): waves * (blocks of the largest split + kFixedBlocks) + kCombineBlocks
-// when a second kernel merges the splits.  A wave holds `per_wave` CTAs: the SM
-// count for plain launches, (clusters the device holds at once) * S for clustered
-// ones, which can be fewer since a cluster's CTAs share one GPC.  The constants are
-// GB300 measurements: the prologue (first gathers, q) and epilogue (partials, merge)
-// of a CTA cost ~2.6 blocks, the combine launch ~0.5 block.
+// resident): waves * (slots of the largest split / 64 + kFixedBlocks) plus the
+// merge: kCombineBlocks for a second kernel, kClusterMergeBlocks per split for the
+// on-chip merge.  A split's slots count fractionally (a latency-bound split of few
+// slots gathers few rows) but at least kMinBlocks.  A wave holds `per_wave` CTAs:
+// the SM count for plain launches, (clusters the device holds at once) * S for
+// clustered ones, which can be fewer since a cluster's CTAs share one GPC.  The
+// constants are GB300 measurements: the prologue (first gathers, q) and epilogue
+// of a CTA cost ~2.6 blocks, the combine launch ~0.5 block, the on-chip merge
+// ~0.05 block per split of the cluster.
 constexpr double kFixedBlocks = 2.6;
 constexpr double kCombineBlocks = 0.5;
+constexpr double kClusterMergeBlocks = 0.05;
+constexpr double kMinBlocks = 0.5;
 
 double step_cost(const smla_params* p, int s, int64_t per_wave, bool fused) {
   const int groups = p->num_heads > 64 ? p->num_heads / 64 : 1;
   const int64_t ctas = static_cast<int64_t>(p->batch) * groups * s;
   const int granules = (p->topk + 15) / 16;
   const int gmax = (granules + s - 1) / s;                // granules of the largest split
-  const int blocks = (gmax * 16 + 63) / 64;
+  const double blocks = std::max(gmax * 16 / 64.0, kMinBlocks);
   const int64_t waves = (ctas + per_wave - 1) / std::max<int64_t>(per_wave, 1);
-  return static_cast<double>(waves) * (blocks + kFixedBlocks) + (fused ? 0.0 : kCombineBlocks);
+  return static_cast<double>(waves) * (blocks + kFixedBlocks) +
+         (fused ? kClusterMergeBlocks * s : kCombineBlocks);
 }
 
 // Cost of S splits in the cheaper of the two launch forms; *fused tells which.
