@@ -17,37 +17,45 @@
 // split-K scheme of "The 80KB Mystery: Resolving Contradictory Evidence in Triton
 // Kernel Optimization", section "The Context: Optimizing Attention on Blackwell").
 // Launched as thread-block clusters of the S splits of a (query, head group), the
-// CTAs then also merge the splits after a cluster barrier, each for a slice of the
-// heads, and write the final out and lse.
+// CTAs keep their partials in shared memory and, after a cluster barrier, each merges
+// a slice of the heads from the other splits' shared memory and writes the final out
+// and lse.
 //
-// Stacked blocks.  A block of 64 tokens is held as a 128-row operand: row t (< 64)
-// holds token t's columns 0..255, row 64 + t its columns 256..511 (nope 256..447 and
-// the rope).  The score MMA runs with M = 128 rows against the query stacked the
-// same way (N = 2 NH: head h's columns 0..255, then again its columns 256..511), so
-// every tcgen05.mma has full height although a block has 64 tokens.  Score row t,
-// column h plus score row 64 + t, column NH + h is the score of token t and head h;
-// the softmax warps add the two halves (each thread owns one tensor-memory lane and
-// trades half of its heads with the thread that holds the other half of its token).
+// Stacked blocks.  A block of 64 tokens is held as a 128-row f16 operand: row t
+// (< 64) holds token t's columns 0..255, row 64 + t its columns 256..511 (nope
+// 256..447 and the rope), so every tcgen05.mma has M = 128 although a block has 64
+// tokens.  The query is stacked the same way (head h's columns 0..255, then again
+// its columns 256..511); each half of a score is a partial dot product, and the
+// softmax threads holding the two halves add them (trading them through shared
+// memory).
+//   - 16 / 32 heads (Q in shared memory): S^T = K_stacked . Q_stacked^T, tokens as
+//     the MMA's M, N = 2 NH.  A softmax thread owns one token half for all heads.
+//   - 64 heads (Q in tensor memory): S = Q_stacked . K_stacked^T with the stacked
+//     query (2 NH = 128 rows) as the A operand in tensor memory, so shared memory is
+//     not re-read for Q every block.  A softmax thread owns one head half for the
+//     block's tokens; the running max of a head lives in a register.
 // The value product reads the same bytes: value columns 0..127 are slabs 0-1 of rows
 // 0..63, 128..255 slabs 2-3, 256..383 slabs 0-1 of rows 64..127, and 384..447 slab 2
 // of rows 64..127 paired with a constant block whose first column is 1, so output
 // row 448 is sum_t P[t], the softmax denominator, accumulated and rescaled by the
 // tensor core together with O.
 //
-// Pipeline.  Two block buffers: while the tensor core works on one block, the
-// converter warps fill the other.  The tensor core runs QK(i), QK(i+1), PV(i),
-// PV(i+1), QK(i+2), ... so the softmax of a block overlaps the scores of the next.
-// All operands are f16 (fp32 accumulation): e4m3 -> f16 is one conversion and the
-// power-of-two group scale one f16x2 multiply; q and the rope are converted from
-// bf16 (values beyond the f16 range are reported as SMLA_ERR_RANGE).
+// Pipeline.  Two block buffers: while the tensor core and the softmax work on one
+// block, a set of converter warps fills the other.  All operands are f16 (fp32
+// accumulation): e4m3 -> f16 is one conversion and the power-of-two group scale one
+// f16x2 multiply; q and the rope are converted from bf16 (values beyond the f16 range
+// are reported as SMLA_ERR_RANGE).  The running max is raised lazily (headroom 2^15).
 //
-// Warp roles (768 threads, one CTA per SM):
+// Warp roles (768 threads, one CTA per SM, about 161-180 KB of shared memory):
 //   warps 0..3    softmax: one thread per tensor-memory lane; they also convert q
-//   warps 4..19   16 converters: each gathers, dequantises and stores 4 rows of a
-//                 block (8 lanes per row, 16-byte loads), and writes the epilogue
-//   warp 20       allocates tensor memory and issues the score MMAs (one lane)
-//   warp 21       issues the value-product MMAs (one lane)
-//   warps 22..23  idle (their registers go to the other roles)
+//   warps 4..19   16 converters in two sets of 8 (even / odd blocks): each warp
+//                 gathers 8 rows of its set's block as 8-byte words (8 lanes per
+//                 row), dequantises them into the buffer, and writes the epilogue
+//   warp 20       allocates tensor memory and issues the score MMAs (one lane); with
+//                 Q in tensor memory it also issues the value products, in readiness
+//                 order
+//   warp 21       with Q in shared memory: issues the value-product MMAs (one lane)
+//   warps 21..23  otherwise idle (their registers go to the other roles)
 // Every wait is bounded; on timeout the CTA records SMLA_ERR_TIMEOUT in the device
 // status word and leaves through the epilogue.
 #include <cuda_bf16.h>
@@ -97,7 +105,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // the previous value product) happens only when a score passes the max by 2^15
 constexpr float kLazyMax = 15.0f;
 constexpr int kMaxCluster = 8;                  // splits merged on chip (portable cluster size)
-enum : int { kSplitOnly = 0, kMergeL2 = 1 };
+enum : int { kSplitOnly = 0, kMergeCluster = 1 };
 
 // Named barriers (id 0 is __syncthreads).
 enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 = 5 };
@@ -129,15 +137,15 @@ struct Cfg {
   // memory the carve-out leaves L1 too small for the row gathers: measured slower.)
   static constexpr int kNBuf = 2;
   static constexpr int kQOff = kNBuf * kBuf;
-  // P: SS [64 tokens][NH] (MN-major B operand), one buffer; TS [NH heads][64 tokens]
-  // (K-major B operand, 128-byte rows), two buffers with two block buffers, one with
-  // three (shared memory)
+  // P: SS [64 tokens][NH] (MN-major B operand); TS [NH heads][64 tokens] (K-major B
+  // operand, 128-byte rows).  One buffer, free again once the block's value product
+  // is done.
   static constexpr int kPOff = kTS ? kNBuf * kBuf : kQOff + 4 * kQSlab;
   static constexpr int kPRow = 2 * NH;                     // bytes of one P row (SS: token)
   static constexpr int kPBytes = kBlk * kPRow;
   static constexpr int kPStride = ((kPBytes + 1023) / 1024) * 1024;
-  // one P buffer: keeps the 64-head CTA under ~163 KB, where the carve-out leaves
-  // 92 KB of L1 for the row gathers
+  // (a second P buffer would take the 64-head CTA past ~163 KB, where the carve-out
+  // still leaves 92 KB of L1 for the row gathers)
   static constexpr int kPBufs = 1;
   static constexpr int kXOff = kPOff + kPBufs * kPStride;
   // SS: score halves traded, and the block-max transpose (NH heads x 65 floats);
@@ -153,8 +161,8 @@ struct Cfg {
   static constexpr int kTaddrOff = kBarOff + 8 * B_COUNT;  // uint32
   static constexpr int kAbortOff = kTaddrOff + 4;          // int
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
-  // TS: Q (128 columns), S^T (128), O^T (4 x NH); SS: S^T (two buffers of 2 NH
-  // columns) and O^T (4 x NH)
+  // TS: Q (128 columns), S (128: stacked heads x tokens), O^T (4 x NH); SS: S^T (two
+  // buffers of 2 NH columns) and O^T (4 x NH)
   static constexpr uint32_t kTmemCols = kTS ? 512 : 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
   static constexpr uint32_t kTQ = 0, kTS_S = kTS ? 128 : 0, kTO = kTS ? 256 : 4 * NH;
   static constexpr uint32_t kPSwz = NH == 64 ? SWZ_128B : NH == 32 ? SWZ_64B : SWZ_32B;
@@ -216,11 +224,6 @@ __device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
                : "=r"(v.x), "=r"(v.y)
                : "l"(p));
   return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
 }
 // Named-barrier helpers: `count` threads meet at barrier `id`.
 __device__ __forceinline__ void bar_sync(int id, int count) {
@@ -478,10 +481,11 @@ __device__ __forceinline__ bool scales_fast(uint32_t lo, uint32_t hi) {
 }
 
 // MODE kSplitOnly: writes the split's normalised partial O and lse (o_part, lse_part).
-// MODE kMergeL2: launched as clusters of the S splits of one (query, head group); each
-//   split writes its partials as above, then after a cluster barrier each CTA merges
-//   a slice of the heads from the (L2-resident) partials of all the splits and writes
-//   the final bf16 out and lse: the split-K combine without a second launch.
+// MODE kMergeCluster: launched as clusters of the S splits of one (query, head group);
+//   each split keeps its partial in shared memory, then after a cluster barrier each
+//   CTA merges a slice of the heads from all the splits' shared memory (distributed
+//   shared memory) and writes the final bf16 out and lse: the split-K combine without
+//   a second launch and without partials in global memory.
 template <int NH, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ kv,
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();
   grid_dep_launch();
   // SS: S^T buffer u at columns [2 NH u, 2 NH (u + 1)), O^T block mb at 4 NH + mb NH;
-  // TS: Q at 0..127, S^T at 128..255, O^T block mb at 256 + mb NH
+  // TS: Q at 0..127, S at 128..255, O^T block mb at 256 + mb NH
   const uint32_t tQ = tmem + C::kTQ;
   const uint32_t tS = tmem + C::kTS_S;
   const uint32_t tO = tmem + C::kTO;
@@ -718,9 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!C::kTS && qk_issuer && lane == 0 && nb > 0)
       mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
-    // the cluster barrier of the merging epilogue, in step with the other roles
     // the two cluster barriers of the merging epilogue, in step with the other roles
-    if constexpr (MODE == kMergeL2) {
+    if constexpr (MODE == kMergeCluster) {
       cluster_sync();
       cluster_sync();
     }
@@ -1106,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bar_sync(kBarEpi, kSoftWarps * 32 + kConv);
     // the two cluster barriers of the merging epilogue, in step with the other roles
-    if constexpr (MODE == kMergeL2) {
+    if constexpr (MODE == kMergeCluster) {
       cluster_sync();
       cluster_sync();
     }
@@ -1262,7 +1265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < NH; ++k) lfin[k] = o[k];
     }
-    if constexpr (MODE == kMergeL2) {
+    if constexpr (MODE == kMergeCluster) {
       if (d < kNope) {
 #pragma unroll
         for (int k = 0; k < NH; ++k) o_s[k * kNope + d] = o[k];
@@ -1273,7 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = lfin[wt];
       const float lse = lt > 0.f ? (mbuf[wt] + log2f(lt)) * kLn2 : -INFINITY;
       const float ri = lt > 0.f ? 1.0f / lt : 0.f;
-      if constexpr (MODE == kMergeL2) {   // read by the other splits of the cluster
+      if constexpr (MODE == kMergeCluster) {   // read by the other splits of the cluster
         lse_s[wt] = lse;
         rinv_s[wt] = ri;
       } else {
@@ -1281,7 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rinv[wt] = ri;
       }
     }
-    if constexpr (MODE != kMergeL2) {
+    if constexpr (MODE != kMergeCluster) {
       bar_sync(kBarConv, kConv);
       if (d < kNope) {
         const int64_t hstride = static_cast<int64_t>(S) * kNope;
@@ -1290,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < NH; ++k) dst[k * hstride] = o[k] * rinv[k];
       }
     }
-    if constexpr (MODE == kMergeL2) {
+    if constexpr (MODE == kMergeCluster) {
       cluster_sync();   // every split of this (query, head group) holds its partial
       // This CTA merges heads [h_lo, h_hi), reading the other splits' partials from
       // their shared memory (split r is cluster rank r): weights exp(lse_r - lse) / l_r.
@@ -1527,13 +1530,13 @@ cudaError_t launch_decode_fused(const void* q, const void* kv, const int32_t* in
                                 float softmax_scale, cudaStream_t stream) {
   switch (H) {
     case 16:
-      return launch_fused_t<16, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+      return launch_fused_t<16, kMergeCluster>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
                                           S, num_rows, stride, softmax_scale, stream);
     case 32:
-      return launch_fused_t<32, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+      return launch_fused_t<32, kMergeCluster>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
                                           S, num_rows, stride, softmax_scale, stream);
     default:
-      return launch_fused_t<64, kMergeL2>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
+      return launch_fused_t<64, kMergeCluster>(q, kv, indices, o_part, lse_part, out, lse, B, H, topk,
                                           S, num_rows, stride, softmax_scale, stream);
   }
 }
@@ -1543,9 +1546,9 @@ cudaError_t fused_clusters(int H, int S, int* clusters) {
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   switch (H) {
-    case 16: return cluster_count<16, kMergeL2>(dev, S, clusters);
-    case 32: return cluster_count<32, kMergeL2>(dev, S, clusters);
-    default: return cluster_count<64, kMergeL2>(dev, S, clusters);
+    case 16: return cluster_count<16, kMergeCluster>(dev, S, clusters);
+    case 32: return cluster_count<32, kMergeCluster>(dev, S, clusters);
+    default: return cluster_count<64, kMergeCluster>(dev, S, clusters);
   }
 }
 
