@@ -58,10 +58,12 @@
 //   warps 21..23  otherwise idle (their registers go to the other roles)
 // Every wait is bounded; on timeout the CTA records SMLA_ERR_TIMEOUT in the device
 // status word and leaves through the epilogue.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/smla.h"
@@ -86,6 +88,7 @@ constexpr int kConvWarp0 = 4;
 constexpr int kConvWarps = 16;
 constexpr int kConv = kConvWarps * 32;          // 512
 constexpr int kMmaWarp = 20;
+constexpr int kTmaWarp = 22;                    // issues the row gathers (tensor copies)
 constexpr int kThreads = 24 * 32;               // 768
 // Register split (setmaxnreg): launched with kLaunchRegs per thread (65536 / 768
 // rounded down to a multiple of 8); the MMA warpgroup gives registers back, the
@@ -105,6 +108,19 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // the previous value product) happens only when a score passes the max by 2^15
 constexpr float kLazyMax = 15.0f;
 constexpr int kMaxCluster = 8;                  // splits merged on chip (portable cluster size)
+// Row gather by tensor copies (Q in tensor memory).  The rows of half a block (32
+// slots) land in one stage of a ring, as 592-byte windows (74 words of 8 bytes: the row
+// and 8 bytes before or after it), four rows per copy; the four windows of a copy land
+// back to back in a 2432-byte group (a multiple of 128 bytes).  The rows are split by
+// the parity of their 16-byte alignment, so a half block takes at most 9 groups.
+constexpr int kHalfRows = 32;
+constexpr int kWinWords = 74;
+constexpr int kWin = kWinWords * 8;             // 592
+constexpr int kGrp = 2432;
+constexpr int kMaxGroups = 9;
+constexpr int kStageBytes = kMaxGroups * kGrp;  // 21888
+constexpr int kStages = 3;
+constexpr uint32_t kNoRow = 0xffffu;            // window offset of a masked slot
 enum : int { kSplitOnly = 0, kMergeCluster = 1 };
 
 // Named barriers (id 0 is __syncthreads).
@@ -118,11 +134,30 @@ enum : int { kBarSoft = 1, kBarConv = 2, kBarEpi = 3, kBarPair0 = 4, kBarPair1 =
 // buffer, PFULL0, with Q in shared memory); ODONE: all value products done (and with
 // them all scores); QDONE: the score MMAs done (drain on abort); QRAW: the bf16 q
 // rows copied into buffer 1 (Q in shared memory); QREADY: the stacked f16 Q and the
-// constant block written.
+// constant block written.  Rows gathered by tensor copies: RAWFULL0..3: the rows of the
+// next half block that converter group g (set g / 2, half g % 2) takes have landed in
+// their stage (one barrier per group, so each is waited in order by one group only);
+// RAWEMPTY0..2: the converters have taken the rows out of stage 0..2.
 enum Bar : int {
   B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_SFULL0, B_SFULL1,
   B_SEMPTY0, B_SEMPTY1,
-  B_PFULL0, B_PFULL1, B_ODONE, B_QDONE, B_QRAW, B_QREADY, B_COUNT
+  B_PFULL0, B_PFULL1, B_ODONE, B_QDONE, B_QRAW, B_QREADY, B_RAWFULL0, B_RAWFULL1, B_RAWFULL2,
+  B_RAWFULL3, B_RAWEMPTY0, B_RAWEMPTY1, B_RAWEMPTY2, B_COUNT
+};
+
+// The tensor maps of one launch.  Rows are gathered through `even` and `odd`: rows are
+// 8-byte aligned and a tensor copy must start on a 16-byte boundary.  With a row stride
+// that is a multiple of 16 every row starts on one and `even` maps them all (x = 0: the
+// row and 8 zero-filled bytes past its 73 words).  Otherwise every other row starts 8
+// bytes past a boundary: `even` then maps row pairs (row 2k at x = 0), `odd` the row
+// pairs shifted by stride - 8 bytes (row 2k + 1 at byte 8 of its window), and split is
+// 1.  `q` maps q as [B H rows][512 bf16] in boxes of 64 columns x NH rows, 128-byte
+// swizzled (16-byte unit u of row r lands at unit u ^ (r % 8) of its 128-byte row).
+struct __align__(64) RowMaps {
+  CUtensorMap even;
+  CUtensorMap odd;
+  CUtensorMap q;
+  int split;
 };
 
 template <int NH>
@@ -133,9 +168,13 @@ struct Cfg {
   static constexpr bool kTS = NH == 64;
   static constexpr int kHalf = NH / 2;                     // heads per softmax thread (SS)
   static constexpr int kQSlab = 2 * NH * 128;              // stacked Q: 2 NH rows x 128 B
-  // Two block buffers.  (A third fits for 16 and 64 heads, but above ~195 KB of shared
-  // memory the carve-out leaves L1 too small for the row gathers: measured slower.)
+  // Two block buffers.  Q in tensor memory: the rows are gathered by tensor copies
+  // into a staging ring, so L1 is not involved and the carve-out may leave it small.
+  // Q in shared memory: the converters load the rows through L1, which above ~195 KB
+  // of shared memory the carve-out leaves too small for them (measured slower).
   static constexpr int kNBuf = 2;
+  // the buffer that holds the bf16 q rows until the softmax warps have converted them
+  static constexpr int kQRawBuf = 1;
   static constexpr int kQOff = kNBuf * kBuf;
   // P: SS [64 tokens][NH] (MN-major B operand); TS [NH heads][64 tokens] (K-major B
   // operand, 128-byte rows).  One buffer, free again once the block's value product
@@ -160,7 +199,12 @@ struct Cfg {
   static constexpr int kBarOff = kAlphaOff + NH * 4;       // uint64 [B_COUNT]
   static constexpr int kTaddrOff = kBarOff + 8 * B_COUNT;  // uint32
   static constexpr int kAbortOff = kTaddrOff + 4;          // int
-  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // + alignment slack
+  // tensor-copy gather: the staging ring, the window offset of each slot's row per
+  // stage, and the map rows in gather order
+  static constexpr int kStageOff = ((kAbortOff + 4 + 1023) / 1024) * 1024;
+  static constexpr int kTabOff = kStageOff + (kTS ? kStages * kStageBytes : 0);  // uint16 [3][32]
+  static constexpr int kListOff = kTabOff + (kTS ? kStages * 2 * kHalfRows : 0);   // int [36]
+  static constexpr int kSmemBytes = kListOff + (kTS ? 4 * (kHalfRows + 4) : 0) + 1024;  // + slack
   // TS: Q (128 columns), S (128: stacked heads x tokens), O^T (4 x NH); SS: S^T (two
   // buffers of 2 NH columns) and O^T (4 x NH)
   static constexpr uint32_t kTmemCols = kTS ? 512 : 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
@@ -207,21 +251,27 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  if (!SMLA_SMEM_OK(addr, 8)) return make_uint2(0u, 0u);
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
   if (!SMLA_SMEM_OK(addr, 8)) return;
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 __device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
   uint2 v;
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
                : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
 }
@@ -443,14 +493,15 @@ __device__ __forceinline__ bool idx_ok(int idx, int64_t num_rows, bool report) {
 }
 
 // ---------------------------------------------------------------------------
-// Row loading.  A row is 73 words of 8 bytes (rows are 8-byte aligned): word w < 56
+// Row words.  A row is 73 words of 8 bytes (rows are 8-byte aligned): word w < 56
 // holds nope columns 8w..8w+7 (scale group w / 8), word 56 the 7 scales and the pad,
 // words 57..72 the rope.  8 lanes share a row (lane = 8 * row + q); lane q reads words
-// q + 8k into register slot k (k = 0..8, and k = 9 for word 72 on lane 0), so slot
-// k < 7 of every lane is a nope word of group k, slot 7 is the scale word (lane 0) or
-// rope word 56 + q, slot 8 rope word 64 + q.  A 16-byte shared store of slot k by a
-// warp is served in four phases of 8 consecutive lanes, i.e. one row each, whose 8
-// words fill the 8 distinct 16-byte units of their 128-byte row: no bank conflicts.
+// q + 8k of the row (gathered, or from the cache) into register slot k (k = 0..8, and
+// k = 9 for word 72 on lane 0), so slot k < 7 of every lane is a nope word of group k, slot 7 is the scale
+// word (lane 0) or rope word 56 + q, slot 8 rope word 64 + q.  A 16-byte shared store
+// of slot k by a warp is served in four phases of 8 consecutive lanes, i.e. one row
+// each, whose 8 words fill the 8 distinct 16-byte units of their 128-byte row: no bank
+// conflicts.
 // ---------------------------------------------------------------------------
 constexpr int kSlots = 10;
 
@@ -489,10 +540,10 @@ __device__ __forceinline__ bool scales_fast(uint32_t lo, uint32_t hi) {
 template <int NH, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     split_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ kv,
-                 const int32_t* __restrict__ indices, float* __restrict__ o_part,
-                 float* __restrict__ lse_part, __nv_bfloat16* __restrict__ out,
-                 float* __restrict__ lse_out, int H, int topk, int S, int64_t num_rows,
-                 int64_t stride, float scale_log2, int fault_block) {
+                 const __grid_constant__ RowMaps rows, const int32_t* __restrict__ indices,
+                 float* __restrict__ o_part, float* __restrict__ lse_part,
+                 __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out, int H, int topk,
+                 int S, int64_t num_rows, int64_t stride, float scale_log2, int fault_block) {
   using C = Cfg<NH>;
   constexpr int HH = C::kHalf;
   extern __shared__ uint8_t smem_raw[];
@@ -526,6 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_QDONE), 1);
     mbar_init(bar(B_QRAW), 1);
     mbar_init(bar(B_QREADY), kSoftWarps);
+    for (int i = B_RAWFULL0; i <= B_RAWFULL3; ++i) mbar_init(bar(i), 1);
+    for (int i = B_RAWEMPTY0; i <= B_RAWEMPTY2; ++i) mbar_init(bar(i), kConvWarps / 4);
     *abort_f = 0;
     fence_mbar_init();
   }
@@ -559,15 +612,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kTwoIssuers = !C::kTS;
     const bool qk_issuer = warp == kMmaWarp, pv_issuer = kTwoIssuers && warp == kMmaWarp + 1;
     if ((qk_issuer || pv_issuer) && lane == 0 && nb > 0) {
-      // SS: the bf16 q rows h0..h0+NH-1 (contiguous, NH KB) into block buffer 1, where
-      // the softmax warps convert them into the stacked Q operand.
-      if (!C::kTS && qk_issuer) {
-        const uint8_t* src =
-            reinterpret_cast<const uint8_t*>(q + (static_cast<int64_t>(b) * H + h0) * kQkDim);
+      // The bf16 q rows h0..h0+NH-1 (NH KB) into block buffer kQRawBuf, where the
+      // softmax warps convert them into the stacked Q operand: SS as they are
+      // (contiguous rows), TS as 8 swizzled boxes of 64 columns (box c at c NH 128
+      // bytes).
+      if (qk_issuer) {
         mbar_arrive_expect_tx(bar(B_QRAW), NH * 1024);
+        if constexpr (C::kTS) {
 #pragma unroll
-        for (int k = 0; k < NH / 16; ++k)
-          bulk_g2s(sbase + kBuf + k * 16384, src + k * 16384, 16384, bar(B_QRAW));
+          for (int c = 0; c < 8; ++c)
+            tma_load_2d(sbase + C::kQRawBuf * kBuf + c * NH * 128, &rows.q, 64 * c, b * H + h0,
+                        bar(B_QRAW));
+        } else {
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(q + (static_cast<int64_t>(b) * H + h0) * kQkDim);
+#pragma unroll
+          for (int k = 0; k < NH / 16; ++k)
+            bulk_g2s(sbase + C::kQRawBuf * kBuf + k * 16384, src + k * 16384, 16384, bar(B_QRAW));
+        }
       }
       // SS: S^T (tokens x stacked heads) = stacked K . stacked Q^T, both from shared
       // memory; TS: S (stacked heads x stacked tokens) = Q (tensor memory) . K^T.
@@ -718,8 +780,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
       }
     }
-    // the bulk copy of q has landed before the CTA can leave
-    if (!C::kTS && qk_issuer && lane == 0 && nb > 0)
+    if (C::kTS && warp == kTmaWarp && nb > 0) {
+      // ===================== row gather =====================
+      // Half block h (slots 32h .. 32h + 31 of the split) into stage h % kStages, once
+      // the converters have taken half block h - kStages out of it.  Lane l handles
+      // slot l: the valid rows are ordered even-map rows first, then odd-map rows, each
+      // run padded to a multiple of 4 with a copy of its first row, and lane g issues
+      // the copy of rows 4g..4g+3.  A masked slot (index -1, past the split, or out of
+      // range: reported) is not gathered; its window offset is kNoRow.  Converter
+      // group 2 (h / 2 % 2) + h % 2 takes half block h.
+      if (lane == 0) {
+        prefetch_tensormap(&rows.even);
+        prefetch_tensormap(&rows.odd);
+      }
+      uint16_t* tab = reinterpret_cast<uint16_t*>(smem + C::kTabOff);
+      int* list = reinterpret_cast<int*>(smem + C::kListOff);
+      const uint32_t stage0 = sbase + C::kStageOff;
+      const uint32_t lt = (1u << lane) - 1u;
+      const bool split = rows.split != 0;
+      const int nh = 2 * nb;
+      // the indices of the next four half blocks are in flight (a load's latency is
+      // longer than a half block's turn when its stage is free)
+      auto half_idx = [&](int hx) {
+        return hx < nh ? raw_idx(idx_row, sp.t_begin + hx * kHalfRows + lane, sp.t_end) : -1;
+      };
+      int r1 = half_idx(0), r2 = half_idx(1), r3 = half_idx(2), r4 = half_idx(3);
+      int issued = 0;
+#pragma unroll 1
+      for (int h = 0; h < nh; ++h) {
+        const int st = h % kStages;
+        const int r = r1;
+        r1 = r2;
+        r2 = r3;
+        r3 = r4;
+        r4 = half_idx(h + 4);
+        const bool v = idx_ok(r, num_rows, true);
+        const bool o = split && (r & 1);
+        const uint32_t e = __ballot_sync(0xffffffffu, v && !o);
+        const uint32_t d = __ballot_sync(0xffffffffu, v && o);
+        const int ne = __popc(e), nep = (ne + 3) & ~3;
+        const int no = __popc(d), nop = (no + 3) & ~3;
+        const int p = !v ? -1 : o ? nep + __popc(d & lt) : __popc(e & lt);
+        const int m = split ? r >> 1 : r;   // map row
+        if (h >= kStages && !warp_wait(bar(B_RAWEMPTY0 + st), (h / kStages - 1) & 1, abort_f, limit))
+          break;
+        tab[st * kHalfRows + lane] =
+            p < 0 ? static_cast<uint16_t>(kNoRow)
+                  : static_cast<uint16_t>((p >> 2) * kGrp + (p & 3) * kWin + (o ? 8 : 0));
+        if (p >= 0) list[p] = m;
+        __syncwarp();
+        if (lane < nep - ne) list[ne + lane] = list[0];
+        if (lane < nop - no) list[nep + no + lane] = list[nep];
+        __syncwarp();
+        const int ng = (nep + nop) >> 2;
+        const uint32_t full = bar(B_RAWFULL0 + 2 * ((h >> 1) & 1) + (h & 1));
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(ng * 4 * kWin));
+        __syncwarp();
+        if (lane < ng) {
+          const bool odd_map = 4 * lane >= nep;
+          int g[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            g[k] = list[4 * lane + k];
+#ifdef SMLA_DEBUG
+            // the map row lies inside its map (a row out of range is not copied:
+            // row 0 stands in, so the byte count stays right)
+            const int64_t extent = !split ? num_rows : odd_map ? num_rows / 2 : (num_rows + 1) / 2;
+            if (g[k] < 0 || g[k] >= extent) {
+              record_status(SMLA_ERR_INTERNAL);
+              g[k] = 0;
+            }
+#endif
+          }
+          tma_gather4(stage0 + static_cast<uint32_t>(st * kStageBytes + lane * kGrp),
+                      odd_map ? &rows.odd : &rows.even, 0, g[0], g[1], g[2], g[3], full);
+        }
+        __syncwarp();
+        issued = h + 1;
+      }
+      // Every copy has landed before the CTA can leave.  The halves before the last
+      // kStages were taken by the converters (their stages were reused), so only the
+      // last kStages can still be in flight; each is the latest phase of its group's
+      // barrier.
+      if (lane == 0) {
+        for (int h = max(0, issued - kStages); h < issued; ++h)
+          mbar_wait(bar(B_RAWFULL0 + 2 * ((h >> 1) & 1) + (h & 1)), (h >> 2) & 1,
+                    static_cast<long long>(kWaitLimitK) << 10);
+      }
+      __syncwarp();
+    }
+    // the copy of q has landed before the CTA can leave
+    if (qk_issuer && lane == 0 && nb > 0)
       mbar_wait(bar(B_QRAW), 0, static_cast<long long>(limit) << 10);
     __syncwarp();
     // the two cluster barriers of the merging epilogue, in step with the other roles
@@ -743,24 +894,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = nb > 0;
     if (ok) {
       // ---- q row h, columns 256 half .. +255 (bf16) -> f16 pairs in columns 0..127 of
-      // this lane: the stacked Q operand; then the constant block of the value product
-      const uint4* src = reinterpret_cast<const uint4*>(
-          q + (static_cast<int64_t>(b) * H + h0 + h) * kQkDim + 256 * half);
+      // this lane: the stacked Q operand; then the constant block of the value product.
+      // Phase ph reads box 4 half + ph (64 columns): unit u of row h at u ^ (h % 8).
+      ok = group_wait(bar(B_QRAW), 0, abort_f, limit, poller, kBarSoft, 128);
       bool q_bad = false;
-      uint4 c4[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) c4[k] = ldg_nc_u4(src + k);
+      const uint32_t qrow = sbase + C::kQRawBuf * kBuf + static_cast<uint32_t>(h) * 128;
+      const uint32_t qsw = static_cast<uint32_t>(h & 7);
 #pragma unroll 1
-      for (int ph = 0; ph < 4; ++ph) {
-        uint4 n4[8];
-        if (ph < 3) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) n4[k] = ldg_nc_u4(src + 8 * (ph + 1) + k);
-        }
-        float f[32];   // column 32 ph + j: elements 2j, 2j + 1 of the chunk (f16 pair)
+      for (int ph = 0; ok && ph < 4; ++ph) {
+        const uint32_t box = qrow + static_cast<uint32_t>((4 * half + ph) * NH * 128);
+        float f[32];   // column 32 ph + j: elements 2j, 2j + 1 of the box row (f16 pair)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t w[4] = {c4[k].x, c4[k].y, c4[k].z, c4[k].w};
+          const uint4 c4 = ld_shared_v4(box + ((static_cast<uint32_t>(k) ^ qsw) << 4));
+          const uint32_t w[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t hv = bf16x2_to_f16x2(w[j]);
@@ -770,10 +917,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st16(tQ + lane_base + 32 * ph, f);
         tmem_st16(tQ + lane_base + 32 * ph + 16, f + 16);
-        if (ph < 3) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) c4[k] = n4[k];
-        }
       }
       tmem_wait_st();
       if (q_bad) record_status(SMLA_ERR_RANGE);
@@ -942,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
         for (int k = 0; k < NH * 64 / 128; ++k) {
           const int ui = tid + 128 * k, h = ui >> 6, u = ui & 63;
-          const uint4 v = ld_shared_v4(sbase + kBuf + ui * 16);
+          const uint4 v = ld_shared_v4(sbase + C::kQRawBuf * kBuf + ui * 16);
           const uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                      bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
           q_bad |= f16x2_has_inf_or_nan(o.x) | f16x2_has_inf_or_nan(o.y) |
@@ -1117,9 +1260,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConv) : "memory");
     // ===================== converters =====================
     // Two sets of 8 warps: set 0 fills buffer 0 with the even blocks, set 1 buffer 1
-    // with the odd blocks.  A warp converts 8 rows of its block (two quads of 4 rows,
-    // 8 lanes per row) from registers, then loads the same rows of its next block
-    // (two blocks on), so each warp has only one block of loads in flight.
+    // with the odd blocks.  A warp converts 8 rows of its block (two quads of 4 rows, 8
+    // lanes per row) from registers, then fetches the same rows of its next block (two
+    // blocks on) into registers, so each warp holds one block ahead:
+    //   Q in tensor memory: out of the staging ring (gathered by tensor copies), which
+    //   frees the stage for another gather; warps 0-3 of a set (group 2 set) take the
+    //   first half of each block, warps 4-7 (group 2 set + 1) the second;
+    //   Q in shared memory: by its own loads from the cache.
     const int cw = warp - kConvWarp0;            // 0..15
     const int wt = tid - kConvWarp0 * 32;        // 0..511
     const int set = cw >> 3;
@@ -1127,8 +1274,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb0 = 8 * (cw & 7) + (lane >> 3);  // row of quad 0 (quad 1: + 4)
     const int row_lane0 = lane & ~7;             // lane q = 0 of this row (holds the scales)
     uint2 c[2][kSlots];                          // [quad][slot]
-    int nraw[2] = {-1, -1};                      // stored indices of the rows, 2 blocks ahead
     bool ok = set < nb;
+    const int hq = (cw >> 2) & 1;                // half of the block this warp takes
+    const uint16_t* tab = reinterpret_cast<const uint16_t*>(smem + C::kTabOff);
+    // Q in tensor memory: block i's rows from its stage into c (a masked slot reads as
+    // zeros)
+    auto take_rows = [&](int i) -> bool {
+      const int h = 2 * i + hq, st = h % kStages;
+      if (!warp_wait(bar(B_RAWFULL0 + 2 * set + hq), (i >> 1) & 1, abort_f, limit)) return false;
+      const uint32_t stage = sbase + C::kStageOff + static_cast<uint32_t>(st * kStageBytes);
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t off = tab[st * kHalfRows + rb0 - kHalfRows * hq + 4 * g];
+        const uint32_t a = stage + off + 8u * static_cast<uint32_t>(q8);
+        const bool has = off != kNoRow;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) c[g][k] = has ? ld_shared_v2(a + 64u * k) : make_uint2(0u, 0u);
+        c[g][9] = has && q8 == 0 ? ld_shared_v2(a + 576u) : make_uint2(0u, 0u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_RAWEMPTY0 + st));
+      return true;
+    };
+    // Q in shared memory: rows loaded from the cache
+    int nraw[2] = {-1, -1};                      // stored indices of the rows, 2 blocks ahead
     auto row_of = [&](int raw, bool report) -> const uint8_t* {
       if (!idx_ok(raw, num_rows, report)) return nullptr;
 #ifdef SMLA_DEBUG
@@ -1150,7 +1319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         nraw[g] = raw_idx(idx_row, sp.t_begin + (i + 2) * kBlk + rb0 + 4 * g, sp.t_end);
       }
     };
-    if (ok) {
+    if (C::kTS && ok) {
+      ok = take_rows(set);
+    } else if (ok) {
 #pragma unroll
       for (int g = 0; g < 2; ++g)
         nraw[g] = raw_idx(idx_row, sp.t_begin + set * kBlk + rb0 + 4 * g, sp.t_end);
@@ -1213,12 +1384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int i = set; ok && i < nb; i += 2) {
       const int u = i % C::kNBuf;
-      // buffer u is free once the value product of block i - kNBuf is done; buffer 1
-      // first holds the staged q rows (Q in shared memory) until the softmax warps
-      // have converted them
+      // buffer u is free once the value product of block i - kNBuf is done; buffer
+      // kQRawBuf first holds the staged q rows until the softmax warps have converted
+      // them
       if (i >= C::kNBuf)
         ok = warp_wait(bar(B_EMPTY0 + u), ((i / C::kNBuf) - 1) & 1, abort_f, limit);
-      else if (i == 1 && !C::kTS)
+      else if (i == C::kQRawBuf)
         ok = warp_wait(bar(B_QREADY), 0, abort_f, limit);
       if (!ok) break;
       convert(c[0], 0, i);
@@ -1227,7 +1398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       // (the test hook withholds one warp's arrival, so the MMA warp's wait runs out)
       if (lane == 0 && !(i == fault_block && (cw & 7) == 0)) mbar_arrive(bar(B_FULL0 + u));
-      if (i + 2 < nb) load_rows(i + 2);
+      if (i + 2 < nb) {
+        if constexpr (C::kTS)
+          ok = take_rows(i + 2);
+        else
+          load_rows(i + 2);
+      }
     }
 
     // ===================== epilogue =====================
@@ -1409,6 +1585,63 @@ cudaError_t configure(int dev) {
   return cudaSuccess;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (the
+// library does not link against the driver library).
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &found) != cudaSuccess ||
+        found != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// The tensor maps of a launch: the gather maps of a cache of num_rows (>= 1) rows,
+// `stride` bytes apart (a multiple of 8, >= 584), starting at the 16-byte aligned kv
+// (elements of 8 bytes, boxes of one 74-word window), and the map of the 16-byte
+// aligned q [q_rows][512] bf16 (boxes of 64 columns x nh rows, 128-byte swizzle).
+cudaError_t row_maps(const void* kv, int64_t num_rows, int64_t stride, const void* q,
+                     int64_t q_rows, int nh, RowMaps* m) {
+  const EncodeTiledFn encode = encode_tiled();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  std::memset(static_cast<void*>(m), 0, sizeof(RowMaps));
+  const bool split = (stride % 16) != 0;
+  const cuuint64_t pitch[1] = {static_cast<cuuint64_t>(split ? 2 * stride : stride)};
+  const cuuint32_t box[2] = {kWinWords, 1};
+  const cuuint32_t step[2] = {1, 1};
+  auto make = [&](CUtensorMap* map, const uint8_t* base, cuuint64_t words, cuuint64_t rows_) {
+    const cuuint64_t dim[2] = {words, rows_};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(base), dim, pitch,
+                  box, step, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  const uint8_t* base = static_cast<const uint8_t*>(kv);
+  // even: the row's 73 words (the window's last word lies past the extent: zero-filled)
+  if (make(&m->even, base, kRowBytes / 8, split ? (num_rows + 1) / 2 : num_rows) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (split && num_rows >= 2) {
+    // odd: the window of row 2k + 1 starts 8 bytes before the row and ends with it
+    if (make(&m->odd, base + stride - 8, kWinWords, num_rows / 2) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    m->odd = m->even;
+  }
+  m->split = split ? 1 : 0;
+  const cuuint64_t qdim[2] = {static_cast<cuuint64_t>(kQkDim), static_cast<cuuint64_t>(q_rows)};
+  const cuuint64_t qpitch[1] = {static_cast<cuuint64_t>(kQkDim * 2)};
+  const cuuint32_t qbox[2] = {64, static_cast<cuuint32_t>(nh)};
+  if (encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), qdim, qpitch, qbox,
+             step, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 template <int NH>
 cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices, float* o_part,
                            float* lse_part, int B, int H, int topk, int S, int64_t num_rows,
@@ -1419,11 +1652,14 @@ cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices
   if (e != cudaSuccess) return e;
   e = configure<NH, kSplitOnly>(dev);
   if (e != cudaSuccess) return e;
+  RowMaps maps;
+  e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
+  if (e != cudaSuccess) return e;
   const dim3 grid(S, H / NH, B);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_programmatic(split_kernel<NH, kSplitOnly>, grid, dim3(kThreads), C::kSmemBytes,
                              stream, static_cast<const uint16_t*>(q),
-                             static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
+                             static_cast<const uint8_t*>(kv), maps, indices, o_part, lse_part,
                              static_cast<__nv_bfloat16*>(nullptr), static_cast<float*>(nullptr), H,
                              topk, S, num_rows, stride, scale_log2,
                              g_fault_block.load(std::memory_order_relaxed));
@@ -1485,6 +1721,9 @@ cudaError_t launch_fused_t(const void* q, const void* kv, const int32_t* indices
   e = cluster_fits<NH, MODE>(dev, S, &fits);
   if (e != cudaSuccess) return e;
   if (!fits) return cudaErrorNotSupported;
+  RowMaps maps;
+  e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, H / NH, B);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1501,7 +1740,7 @@ cudaError_t launch_fused_t(const void* q, const void* kv, const int32_t* indices
   cfg.numAttrs = 2;
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&cfg, split_kernel<NH, MODE>, static_cast<const uint16_t*>(q),
-                            static_cast<const uint8_t*>(kv), indices, o_part, lse_part,
+                            static_cast<const uint8_t*>(kv), maps, indices, o_part, lse_part,
                             static_cast<__nv_bfloat16*>(out), lse, H, topk, S, num_rows, stride,
                             scale_log2, g_fault_block.load(std::memory_order_relaxed));
 }

@@ -104,6 +104,36 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
 }
 
 // ---------------------------------------------------------------------------
+// Tensor (TMA) gather of four rows of a 2-D tensor map: row coordinates r0..r3, the
+// same column coordinate x for all four; the boxes land one after another at
+// dst_smem (128-byte aligned), and their full size is counted on the mbarrier.  The
+// map lives in kernel-parameter (grid-constant) or global memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_gather4(uint32_t dst_smem, const void* map, int x, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst_smem),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+// Tensor (TMA) load of one box of a 2-D tensor map at coordinates (x, y) into
+// dst_smem (aligned as the map's swizzle requires), counted on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst_smem),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Programmatic dependent launch.  A grid launched with programmatic stream
 // serialization may start while the previous grid in the stream is still running;
 // grid_dep_wait returns once that grid has completed and its memory writes are

@@ -128,6 +128,61 @@ def test_kv_row_stride_larger_than_row():
     assert_lse_close(lse, rl)
 
 
+def _padded_cache(kv, stride):
+    wide = torch.full((kv.shape[0], stride), 0xFF, dtype=torch.uint8, device="cuda")
+    wide[:, :584] = kv
+    return wide
+
+
+@pytest.mark.parametrize("H", [64, 16])
+@pytest.mark.parametrize("stride,n", [(584, 501), (584, 500), (584, 2), (584, 1), (600, 333),
+                                      (592, 257), (640, 3)])
+def test_rows_at_the_cache_edges(stride, n, H):
+    """The first and last rows of the cache, of both parities, under each row stride the
+    gather treats differently (a multiple of 16 bytes or 8 past one, odd and even row
+    counts): the last row of an odd-sized cache ends exactly at the cache's end."""
+    w, kv, q0, _ = small_case(1, H, n, 1, seed=stride + n + H)     # a cache of n rows
+    q = torch.cat([q0, small_case(1, H, 1, 1, seed=stride + n + H + 1)[2]])
+    assert kv.shape[0] == n
+    rng = np.random.default_rng(n)
+    k = min(n, 150)
+    rest = [r for r in rng.permutation(n).tolist() if r not in (0, n - 1)]
+    row0 = ([0, n - 1] if n > 1 else [0]) + rest[: k - min(n, 2)]
+    idx = np.full((2, k), -1, np.int32)
+    idx[0] = rng.permutation(np.array(row0, np.int32))
+    idx[1, -1] = n - 1                      # one valid slot: the last row, in the last block
+    out, lse = _run(q, _padded_cache(kv, stride), idx)
+    ro, rl = oracle_decode(q, kv, idx)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("pattern", ["even", "odd", "one_odd", "alternating", "three_even"])
+def test_gather_groups_by_row_parity(pattern):
+    """Blocks whose rows are all of one parity, or split 63 / 1, 61 / 3 or evenly:
+    every way the gather's groups of four can be filled and padded."""
+    w, kv, q, _ = small_case(2, 64, 2048, 1, seed=77)
+    n = kv.shape[0]
+    rng = np.random.default_rng(5)
+    ev, od = rng.permutation(np.arange(0, n, 2)), rng.permutation(np.arange(1, n, 2))
+    k = 320
+    if pattern == "even":
+        row = ev[:k]
+    elif pattern == "odd":
+        row = od[:k]
+    elif pattern == "one_odd":          # per block of 64: 63 even, 1 odd
+        row = np.concatenate([np.concatenate([ev[63 * b:63 * b + 63], od[b:b + 1]]) for b in range(5)])
+    elif pattern == "three_even":       # per block: 3 even, 61 odd
+        row = np.concatenate([np.concatenate([od[61 * b:61 * b + 61], ev[3 * b:3 * b + 3]]) for b in range(5)])
+    else:
+        row = np.stack([ev[:k // 2], od[:k // 2]], axis=1).reshape(-1)
+    idx = np.stack([row, row[::-1]]).astype(np.int32)
+    out, lse = _run(q, kv, idx, num_splits=1)        # blocks = slots 64b .. 64b + 63
+    ro, rl = oracle_decode(q, kv, idx)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 def test_deterministic():
     w, kv, q, idx = small_case(4, 64, 5000, 2048, seed=16)
     o1, l1 = _run(q, kv, idx)
