@@ -204,7 +204,9 @@ struct Cfg {
   static constexpr int kStageOff = ((kAbortOff + 4 + 1023) / 1024) * 1024;
   static constexpr int kTabOff = kStageOff + (kTS ? kStages * kStageBytes : 0);  // uint16 [3][32]
   static constexpr int kListOff = kTabOff + (kTS ? kStages * 2 * kHalfRows : 0);   // int [36]
-  static constexpr int kSmemBytes = kListOff + (kTS ? 4 * (kHalfRows + 4) : 0) + 1024;  // + slack
+  // the indices of the next four half blocks (int [4][32])
+  static constexpr int kIdxOff = kListOff + (kTS ? 4 * (kHalfRows + 4) : 0);
+  static constexpr int kSmemBytes = kIdxOff + (kTS ? 4 * 4 * kHalfRows : 0) + 1024;  // + slack
   // TS: Q (128 columns), S (128: stacked heads x tokens), O^T (4 x NH); SS: S^T (two
   // buffers of 2 NH columns) and O^T (4 x NH)
   static constexpr uint32_t kTmemCols = kTS ? 512 : 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
@@ -799,25 +801,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lt = (1u << lane) - 1u;
       const bool split = rows.split != 0;
       const int nh = 2 * nb;
-      // the indices of the next four half blocks are in flight (a load's latency is
-      // longer than a half block's turn when its stage is free)
-      auto half_idx = [&](int hx) {
-        return hx < nh ? raw_idx(idx_row, sp.t_begin + hx * kHalfRows + lane, sp.t_end) : -1;
+      // The indices of the next four half blocks are in flight, copied asynchronously
+      // into a ring of four 32-slot rows (a load's latency is longer than a half
+      // block's turn when its stage is free).
+      int* iring = reinterpret_cast<int*>(smem + C::kIdxOff);
+      auto fetch = [&](int hx) {   // one commit group per half block, empty past the end
+        if (hx < nh) {
+          const int pos = sp.t_begin + hx * kHalfRows + lane;
+          cp_async4(smem_u32(iring + (hx & 3) * kHalfRows + lane),
+                    idx_row + (pos < sp.t_end ? pos : sp.t_begin), pos < sp.t_end ? 4u : 0u);
+        }
+        cp_async_commit();
       };
-      int r1 = half_idx(0), r2 = half_idx(1), r3 = half_idx(2), r4 = half_idx(3);
+      fetch(0);
+      fetch(1);
+      fetch(2);
+      fetch(3);
       int issued = 0;
 #pragma unroll 1
       for (int h = 0; h < nh; ++h) {
         const int st = h % kStages;
-        const int r = r1;
-        r1 = r2;
-        r2 = r3;
-        r3 = r4;
-        r4 = half_idx(h + 4);
+        cp_async_wait<3>();   // half block h's indices have landed
+        const int pos = sp.t_begin + h * kHalfRows + lane;
+        const int r = pos < sp.t_end ? iring[(h & 3) * kHalfRows + lane] : -1;
         const bool v = idx_ok(r, num_rows, true);
         const bool o = split && (r & 1);
         const uint32_t e = __ballot_sync(0xffffffffu, v && !o);
         const uint32_t d = __ballot_sync(0xffffffffu, v && o);
+        fetch(h + 4);         // (r is in use above: its ring row may be refilled)
         const int ne = __popc(e), nep = (ne + 3) & ~3;
         const int no = __popc(d), nop = (no + 3) & ~3;
         const int p = !v ? -1 : o ? nep + __popc(d & lt) : __popc(e & lt);
@@ -858,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         issued = h + 1;
       }
+      cp_async_wait<0>();   // no copy into the ring is left in flight
       // Every copy has landed before the CTA can leave.  The halves before the last
       // kStages were taken by the converters (their stages were reused), so only the
       // last kStages can still be in flight; each is the latest phase of its group's

@@ -129,6 +129,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* map, 
       : "memory");
 }
 
+// Asynchronous 4-byte copy global -> shared (src_bytes 0: the word is zero-filled and
+// nothing is read), grouped by commit_group and awaited by wait_group<n> (all but the
+// n most recent groups of this thread have landed).
+__device__ __forceinline__ void cp_async4(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
