@@ -108,7 +108,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // the previous value product) happens only when a score passes the max by 2^15
 constexpr float kLazyMax = 15.0f;
 constexpr int kMaxCluster = 8;                  // splits merged on chip (portable cluster size)
-// Row gather by tensor copies (Q in tensor memory).  The rows of half a block (32
+// Row gather by tensor copies (64 heads).  The rows of half a block (32
 // slots) land in one stage of a ring, as 592-byte windows (74 words of 8 bytes: the row
 // and 8 bytes before or after it), four rows per copy; the four windows of a copy land
 // back to back in a 2432-byte group (a multiple of 128 bytes).  The rows are split by
@@ -166,12 +166,18 @@ struct Cfg {
   // 64 heads, where 2 NH = 128 stacked query rows fill the MMA's M; Q in shared
   // memory (tokens as M) for fewer heads.
   static constexpr bool kTS = NH == 64;
+  // rows gathered by tensor copies into a staging ring, else by the converters' loads
+  // through L1.  Measured: with 64 heads the tensor copies are faster (the loads
+  // congest the load/store path the softmax warps use); with 16 heads, where the
+  // gather rate bounds the kernel, the loads of all 16 converter warps are (the
+  // tensor-copy unit moves ~13.5 bytes per clock per SM on these rows).
+  static constexpr bool kTmaRows = NH == 64;
   static constexpr int kHalf = NH / 2;                     // heads per softmax thread (SS)
   static constexpr int kQSlab = 2 * NH * 128;              // stacked Q: 2 NH rows x 128 B
-  // Two block buffers.  Q in tensor memory: the rows are gathered by tensor copies
-  // into a staging ring, so L1 is not involved and the carve-out may leave it small.
-  // Q in shared memory: the converters load the rows through L1, which above ~195 KB
-  // of shared memory the carve-out leaves too small for them (measured slower).
+  // Two block buffers.  With kTmaRows the rows are gathered by tensor copies into a
+  // staging ring, so L1 is not involved and the carve-out may leave it small;
+  // otherwise the converters load the rows through L1, which above ~195 KB of shared
+  // memory the carve-out leaves too small for them (measured slower).
   static constexpr int kNBuf = 2;
   // the buffer that holds the bf16 q rows until the softmax warps have converted them
   static constexpr int kQRawBuf = 1;
@@ -202,11 +208,11 @@ struct Cfg {
   // tensor-copy gather: the staging ring, the window offset of each slot's row per
   // stage, and the map rows in gather order
   static constexpr int kStageOff = ((kAbortOff + 4 + 1023) / 1024) * 1024;
-  static constexpr int kTabOff = kStageOff + (kTS ? kStages * kStageBytes : 0);  // uint16 [3][32]
-  static constexpr int kListOff = kTabOff + (kTS ? kStages * 2 * kHalfRows : 0);   // int [36]
+  static constexpr int kTabOff = kStageOff + (kTmaRows ? kStages * kStageBytes : 0);  // u16 [3][32]
+  static constexpr int kListOff = kTabOff + (kTmaRows ? kStages * 2 * kHalfRows : 0);  // int [36]
   // the indices of the next four half blocks (int [4][32])
-  static constexpr int kIdxOff = kListOff + (kTS ? 4 * (kHalfRows + 4) : 0);
-  static constexpr int kSmemBytes = kIdxOff + (kTS ? 4 * 4 * kHalfRows : 0) + 1024;  // + slack
+  static constexpr int kIdxOff = kListOff + (kTmaRows ? 4 * (kHalfRows + 4) : 0);
+  static constexpr int kSmemBytes = kIdxOff + (kTmaRows ? 4 * 4 * kHalfRows : 0) + 1024;  // + slack
   // TS: Q (128 columns), S (128: stacked heads x tokens), O^T (4 x NH); SS: S^T (two
   // buffers of 2 NH columns) and O^T (4 x NH)
   static constexpr uint32_t kTmemCols = kTS ? 512 : 8 * NH <= 128 ? 128 : 8 * NH <= 256 ? 256 : 512;
@@ -782,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) mbar_wait(bar(B_ODONE), 0, static_cast<long long>(kWaitLimitK) << 10);
       }
     }
-    if (C::kTS && warp == kTmaWarp && nb > 0) {
+    if (C::kTmaRows && warp == kTmaWarp && nb > 0) {
       // ===================== row gather =====================
       // Half block h (slots 32h .. 32h + 31 of the split) into stage h % kStages, once
       // the converters have taken half block h - kStages out of it.  Lane l handles
@@ -1275,10 +1281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // with the odd blocks.  A warp converts 8 rows of its block (two quads of 4 rows, 8
     // lanes per row) from registers, then fetches the same rows of its next block (two
     // blocks on) into registers, so each warp holds one block ahead:
-    //   Q in tensor memory: out of the staging ring (gathered by tensor copies), which
-    //   frees the stage for another gather; warps 0-3 of a set (group 2 set) take the
-    //   first half of each block, warps 4-7 (group 2 set + 1) the second;
-    //   Q in shared memory: by its own loads from the cache.
+    //   kTmaRows (64 heads): out of the staging ring (gathered by tensor copies),
+    //   which frees the stage for another gather; warps 0-3 of a set (group 2 set)
+    //   take the first half of each block, warps 4-7 (group 2 set + 1) the second;
+    //   otherwise (16 and 32 heads): by its own loads from the cache.
     const int cw = warp - kConvWarp0;            // 0..15
     const int wt = tid - kConvWarp0 * 32;        // 0..511
     const int set = cw >> 3;
@@ -1289,7 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = set < nb;
     const int hq = (cw >> 2) & 1;                // half of the block this warp takes
     const uint16_t* tab = reinterpret_cast<const uint16_t*>(smem + C::kTabOff);
-    // Q in tensor memory: block i's rows from its stage into c (a masked slot reads as
+    // kTmaRows: block i's rows from its stage into c (a masked slot reads as
     // zeros)
     auto take_rows = [&](int i) -> bool {
       const int h = 2 * i + hq, st = h % kStages;
@@ -1308,7 +1314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_RAWEMPTY0 + st));
       return true;
     };
-    // Q in shared memory: rows loaded from the cache
+    // otherwise: rows loaded from the cache
     int nraw[2] = {-1, -1};                      // stored indices of the rows, 2 blocks ahead
     auto row_of = [&](int raw, bool report) -> const uint8_t* {
       if (!idx_ok(raw, num_rows, report)) return nullptr;
@@ -1331,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nraw[g] = raw_idx(idx_row, sp.t_begin + (i + 2) * kBlk + rb0 + 4 * g, sp.t_end);
       }
     };
-    if (C::kTS && ok) {
+    if (C::kTmaRows && ok) {
       ok = take_rows(set);
     } else if (ok) {
 #pragma unroll
@@ -1411,7 +1417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (the test hook withholds one warp's arrival, so the MMA warp's wait runs out)
       if (lane == 0 && !(i == fault_block && (cw & 7) == 0)) mbar_arrive(bar(B_FULL0 + u));
       if (i + 2 < nb) {
-        if constexpr (C::kTS)
+        if constexpr (C::kTmaRows)
           ok = take_rows(i + 2);
         else
           load_rows(i + 2);
