@@ -1639,6 +1639,8 @@ cudaError_t row_maps(const void* kv, int64_t num_rows, int64_t stride, const voi
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   const uint8_t* base = static_cast<const uint8_t*>(kv);
+  // indices are int32: rows at or past 2^31 are never gathered, so the maps stop there
+  if (num_rows > (int64_t{1} << 31)) num_rows = int64_t{1} << 31;
   // even: the row's 73 words (the window's last word lies past the extent: zero-filled)
   if (make(&m->even, base, kRowBytes / 8, split ? (num_rows + 1) / 2 : num_rows) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
