@@ -27,7 +27,8 @@
 // tokens.  The query is stacked the same way (head h's columns 0..255, then again
 // its columns 256..511); each half of a score is a partial dot product, and the
 // softmax threads holding the two halves add them (trading them through shared
-// memory).
+// memory; the two halves sit in different warps, since a tensor-memory load takes one
+// column address per warp).
 //   - 16 / 32 heads (Q in shared memory): S^T = K_stacked . Q_stacked^T, tokens as
 //     the MMA's M, N = 2 NH.  A softmax thread owns one token half for all heads.
 //   - 64 heads (Q in tensor memory): S = Q_stacked . K_stacked^T with the stacked
@@ -41,21 +42,26 @@
 // tensor core together with O.
 //
 // Pipeline.  Two block buffers: while the tensor core and the softmax work on one
-// block, a set of converter warps fills the other.  All operands are f16 (fp32
-// accumulation): e4m3 -> f16 is one conversion and the power-of-two group scale one
-// f16x2 multiply; q and the rope are converted from bf16 (values beyond the f16 range
-// are reported as SMLA_ERR_RANGE).  The running max is raised lazily (headroom 2^15).
+// block, a set of converter warps fills the other.  With 64 heads the rows are
+// gathered by TMA tile::gather4 copies into a staging ring of half blocks, a few
+// half blocks ahead of the converters; with 16 / 32 heads the converters load them
+// through L1 themselves, a block ahead.  All operands are f16 (fp32 accumulation):
+// e4m3 -> f16 is one conversion and the power-of-two group scale one f16x2
+// multiply; q and the rope are converted from bf16 (values beyond the f16 range are
+// reported as SMLA_ERR_RANGE).  The running max is raised lazily (headroom 2^15).
 //
-// Warp roles (768 threads, one CTA per SM, about 161-180 KB of shared memory):
+// Warp roles (768 threads, one CTA per SM, 156-223 KB of shared memory):
 //   warps 0..3    softmax: one thread per tensor-memory lane; they also convert q
 //   warps 4..19   16 converters in two sets of 8 (even / odd blocks): each warp
-//                 gathers 8 rows of its set's block as 8-byte words (8 lanes per
-//                 row), dequantises them into the buffer, and writes the epilogue
-//   warp 20       allocates tensor memory and issues the score MMAs (one lane); with
-//                 Q in tensor memory it also issues the value products, in readiness
-//                 order
+//                 takes 8 rows of its set's block as 8-byte words (8 lanes per row)
+//                 out of the staging ring or from the cache, dequantises them into
+//                 the buffer, and writes the epilogue
+//   warp 20       allocates tensor memory, copies q in, and issues the score MMAs
+//                 (one lane); with Q in tensor memory it also issues the value
+//                 products, in readiness order
 //   warp 21       with Q in shared memory: issues the value-product MMAs (one lane)
-//   warps 21..23  otherwise idle (their registers go to the other roles)
+//   warp 22       with 64 heads: gathers the rows (tensor copies)
+//   others        idle (their registers go to the other roles)
 // Every wait is bounded; on timeout the CTA records SMLA_ERR_TIMEOUT in the device
 // status word and leaves through the epilogue.
 #include <cuda.h>
@@ -189,8 +195,8 @@ struct Cfg {
   static constexpr int kPRow = 2 * NH;                     // bytes of one P row (SS: token)
   static constexpr int kPBytes = kBlk * kPRow;
   static constexpr int kPStride = ((kPBytes + 1023) / 1024) * 1024;
-  // (a second P buffer would take the 64-head CTA past ~163 KB, where the carve-out
-  // still leaves 92 KB of L1 for the row gathers)
+  // (a second P buffer measured no faster with 16 heads; with 64 heads the staging
+  // ring takes the room)
   static constexpr int kPBufs = 1;
   static constexpr int kXOff = kPOff + kPBufs * kPStride;
   // SS: score halves traded, and the block-max transpose (NH heads x 65 floats);
