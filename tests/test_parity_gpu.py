@@ -157,6 +157,25 @@ def test_rows_at_the_cache_edges(stride, n, H):
     assert_lse_close(lse, rl)
 
 
+@pytest.mark.parametrize("offset,stride", [(16, 584), (48, 584), (16, 592)])
+def test_cache_view_at_a_16_byte_offset(offset, stride):
+    """A cache that starts 16 or 48 bytes into its allocation (16-byte aligned, as the
+    ABI requires, but not 256): the row maps and the odd-row map's shifted base are
+    then not at an allocation boundary."""
+    w, kv, q, idx = small_case(2, 64, 333, 150, seed=offset + stride)
+    n = kv.shape[0]
+    buf = torch.full((offset + n * stride,), 0xFF, dtype=torch.uint8, device="cuda")
+    view = buf[offset:].view(n, stride)
+    view[:, :584] = kv
+    assert view.data_ptr() % 16 == 0 and view.data_ptr() % 256 != 0
+    idx = idx.copy()
+    idx[0, :2] = [0, n - 1]          # first and last rows of the view
+    out, lse = _run(q, view, idx)
+    ro, rl = oracle_decode(q, kv, idx)
+    assert_out_close(out, ro)
+    assert_lse_close(lse, rl)
+
+
 @pytest.mark.parametrize("pattern", ["even", "odd", "one_odd", "alternating", "three_even"])
 def test_gather_groups_by_row_parity(pattern):
     """Blocks whose rows are all of one parity, or split 63 / 1, 61 / 3 or evenly:
