@@ -282,13 +282,6 @@ __device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
                : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 // Named-barrier helpers: `count` threads meet at barrier `id`.
 __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -371,16 +364,6 @@ __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
   } else {
     static_assert(N == 8, "width");
     tmem_ld<8>(taddr, v);
-  }
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float* v) {
-  if constexpr (N % 16 == 0) {
-#pragma unroll
-    for (int k = 0; k < N / 16; ++k) tmem_st<16>(taddr + 16 * k, v + 16 * k);
-  } else {
-    static_assert(N == 8, "width");
-    tmem_st<8>(taddr, v);
   }
 }
 

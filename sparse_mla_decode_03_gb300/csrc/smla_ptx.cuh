@@ -50,21 +50,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The same test, letting the hardware suspend the thread for up to `ns` nanoseconds
-// while the phase is incomplete (it resumes as soon as the phase completes), so a
-// waiting thread takes no issue slots from the warps doing work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for phase `parity` of the barrier to complete, giving up after
 // `limit_cycles` SM clocks.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit_cycles) {
@@ -207,21 +192,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (16-bit inputs, fp32 accumulate;
-// the input type is set by the instruction descriptor).
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same MMA with each 64-bit descriptor given as two 32-bit halves.  Start-address
-// offsets only change the low half, so a caller can move along a tile with one
-// 32-bit add per operand.
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (16-bit inputs, fp32
+// accumulate; the input type is set by the instruction descriptor), each 64-bit
+// descriptor given as two 32-bit halves.  Start-address offsets only change the low
+// half, so a caller can move along a tile with one 32-bit add per operand.
 __device__ __forceinline__ void mma_f16_ss_hl(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                                uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -312,16 +286,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
-//   bit 15 A major (0 = K, 1 = MN), bit 16 B major, bits 17-22 N >> 3, bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
-         ((static_cast<uint32_t>(M) >> 4) << 24);
-}
-
-// Instruction descriptor, kind::f16 with f16 A/B and fp32 D (A/B format fields 0).
+// Instruction descriptor, kind::f16 with f16 A/B and fp32 D:
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16), bit 15 A
+//   major (0 = K, 1 = MN), bit 16 B major, bits 17-22 N >> 3, bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
