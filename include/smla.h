@@ -116,7 +116,11 @@ int smla_decode_plan(const smla_params* p, int32_t num_splits, int32_t* splits, 
  * One whole decode step: the split-K attention and the merge of its splits, as one
  * clustered launch when smla_decode_plan reports fused, else split + combine kernels
  * (the workspace holds the split partials for the combine kernel; the clustered
- * launch merges on chip and leaves it untouched).
+ * launch merges on chip and leaves it untouched).  With 64 heads per CTA (H = 64 or
+ * 128) the rows and q are read by tensor (TMA) copies whose descriptors are encoded
+ * on the host for each call, through the driver's cuTensorMapEncodeTiled (looked up
+ * once via the runtime); a driver without it, or a cache or q the encoder rejects,
+ * gives SMLA_ERR_CUDA and nothing is launched.
  *   q          bf16  [B, H, 512]  (448 nope | 64 rope), 16-byte aligned
  *   kv_cache   uint8 [num_rows, kv_row_stride], 16-byte aligned, rows as above
  *   indices    int32 [B, topk]    row ids; < 0 = masked slot (shared by all heads)

@@ -1661,9 +1661,12 @@ cudaError_t launch_split_t(const void* q, const void* kv, const int32_t* indices
   if (e != cudaSuccess) return e;
   e = configure<NH, kSplitOnly>(dev);
   if (e != cudaSuccess) return e;
-  RowMaps maps;
-  e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
-  if (e != cudaSuccess) return e;
+  RowMaps maps;   // (read only by the kernels that gather by tensor copies)
+  std::memset(static_cast<void*>(&maps), 0, sizeof(RowMaps));
+  if (C::kTmaRows) {
+    e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
+    if (e != cudaSuccess) return e;
+  }
   const dim3 grid(S, H / NH, B);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_programmatic(split_kernel<NH, kSplitOnly>, grid, dim3(kThreads), C::kSmemBytes,
@@ -1730,9 +1733,12 @@ cudaError_t launch_fused_t(const void* q, const void* kv, const int32_t* indices
   e = cluster_fits<NH, MODE>(dev, S, &fits);
   if (e != cudaSuccess) return e;
   if (!fits) return cudaErrorNotSupported;
-  RowMaps maps;
-  e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
-  if (e != cudaSuccess) return e;
+  RowMaps maps;   // (read only by the kernels that gather by tensor copies)
+  std::memset(static_cast<void*>(&maps), 0, sizeof(RowMaps));
+  if (C::kTmaRows) {
+    e = row_maps(kv, num_rows, stride, q, static_cast<int64_t>(B) * H, NH, &maps);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, H / NH, B);
   cfg.blockDim = dim3(kThreads, 1, 1);
