@@ -713,30 +713,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       if (!kTwoIssuers) {
-        // Issue order decided by readiness: the scores of block nq (its buffer filled,
-        // the scores buffer read by the softmax of block nq - 1; at most one block
-        // ahead of the value products) or the value product of block np (its P
-        // written).  Each barrier is tested without suspending (test_wait), so a late
-        // converter set or a late softmax holds up only its own block.
+        // Issue order decided by readiness: the value product of block np (its P
+        // written) or the scores of block nq (its buffer filled, the scores buffer
+        // read by the softmax of block nq - 1; at most one block ahead of the value
+        // products), the value product first when both are ready (it frees a block
+        // buffer for the converters; measured slightly faster).  Each barrier is
+        // tested without suspending (test_wait), so a late converter set or a late
+        // softmax holds up only its own block.
         ok = wait(B_QREADY, 0);
         int nq = 0, np = 0;
         long long t_idle = clock64();
 #pragma unroll 1
         while (ok && np < nb) {
-          if (nq < nb && nq <= np + 1 &&
-              mbar_test_wait(bar(B_FULL0 + nq % C::kNBuf), (nq / C::kNBuf) & 1) &&
-              (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))) {
-            tc_fence_after();
-            opaque();
-            ok = qk(nq);
-            ++nq;
-            t_idle = clock64();
-          } else if (np < nq && (C::kPBufs == 2 ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
-                                                : mbar_test_wait(bar(B_PFULL0), np & 1))) {
+          if (np < nq && (C::kPBufs == 2 ? mbar_test_wait(bar(B_PFULL0 + (np & 1)), (np >> 1) & 1)
+                                         : mbar_test_wait(bar(B_PFULL0), np & 1))) {
             tc_fence_after();
             opaque();
             ok = pv(np);
             ++np;
+            t_idle = clock64();
+          } else if (nq < nb && nq <= np + 1 &&
+                     mbar_test_wait(bar(B_FULL0 + nq % C::kNBuf), (nq / C::kNBuf) & 1) &&
+                     (nq < 1 || mbar_test_wait(bar(B_SEMPTY0), (nq - 1) & 1))) {
+            tc_fence_after();
+            opaque();
+            ok = qk(nq);
+            ++nq;
             t_idle = clock64();
           } else if (*abort_f) {
             ok = false;
