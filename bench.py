@@ -56,7 +56,7 @@ L2_TURNOVER = 3           # L2 capacities read between two reads of one layer
 # one ncu capture of the decode kernel on the batch-32 workload.  They describe the
 # kernel source they were taken on: with any other source the field is null.
 TRAFFIC_KERNEL_SRC = "sparse_mla_decode_03_gb300/csrc/smla_decode.cu"
-TRAFFIC_SRC_SHA256_16 = "91393c55d39aafbe"
+TRAFFIC_SRC_SHA256_16 = "d623f299c93b8b75"
 TRAFFIC_BYTES = 47548160 + 100352
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0

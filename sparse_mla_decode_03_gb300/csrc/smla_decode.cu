@@ -50,7 +50,7 @@
 // multiply; q and the rope are converted from bf16 (values beyond the f16 range are
 // reported as SMLA_ERR_RANGE).  The running max is raised lazily (headroom 2^15).
 //
-// Warp roles (768 threads, one CTA per SM, 156-223 KB of shared memory):
+// Warp roles (768 threads, one CTA per SM, 155-222 KiB of shared memory):
 //   warps 0..3    softmax: one thread per tensor-memory lane; they also convert q
 //   warps 4..19   16 converters in two sets of 8 (even / odd blocks): each warp
 //                 takes 8 rows of its set's block as 8-byte words (8 lanes per row)
@@ -159,7 +159,7 @@ enum Bar : int {
 // pairs shifted by stride - 8 bytes (row 2k + 1 at byte 8 of its window), and split is
 // 1.  `q` maps q as [B H rows][512 bf16] in boxes of 64 columns x NH rows, 128-byte
 // swizzled (16-byte unit u of row r lands at unit u ^ (r % 8) of its 128-byte row).
-struct __align__(64) RowMaps {
+struct RowMaps {   // (aligned as CUtensorMap requires)
   CUtensorMap even;
   CUtensorMap odd;
   CUtensorMap q;
